@@ -1,0 +1,306 @@
+"""Seeded synthetic workloads for sparse paged attention.
+
+This module only draws data: queries, paged K/V pools, block tables, top-k index lists and
+positions. It holds none of the attention arithmetic, so both the float64 oracle (``oracle/``)
+and the CUDA library (``sparse_paged_attention_gb300``) can be fed from it without sharing code.
+
+Shapes follow the DeepSeek-V4 sparse attention workloads timed on the FreeToken PR 633 page
+("Kernel time" table: 64 heads, head_dim 512, 128-token window, index top-k 512, compress ratio
+r in {4, 128, 0}).  Storage conventions (one kv_head; K and V rows of a token stored next to each
+other) are readings of what the pages leave open:
+
+* pool ``kv``: ``[num_blocks, page_size, 2, head_dim]``; index ``[..., 0, :]`` is K, ``[..., 1, :]``
+  is V. Element type bf16, or e4m3 codes stored as uint8 with fp32 ``k_scale``/``v_scale`` per
+  physical row (``block * page_size + slot``).
+* the window pool holds every token of a sequence at its absolute position, addressed through the
+  sequence's window block table (logical page ``pos // page_size``).
+* the compressed pool holds compressed entry ``j`` of a sequence at logical page ``j // page_size``
+  of its compressed block table; entry ``j`` summarises tokens ``r*j .. r*j + r - 1``.
+* top-k rows list compressed entry indices, padded with -1 at the tail.
+
+Pages that no query of the workload reads, and the spare pages of an oversized pool, are filled with
+NaN (bf16 0x7FC0, e4m3 0x7F, scale NaN) so that a stray read shows up in the output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+BF16_NAN_BITS = 0x7FC0
+E4M3_NAN_CODE = 0x7F
+E4M3_MAX = 448.0
+
+__all__ = [
+    "Pool", "Workload", "build", "make", "CONFIG_NAMES", "bf16_bits", "pool_rows_referenced",
+]
+
+
+@dataclass
+class Pool:
+    """One paged K/V pool plus the block table that maps each sequence's logical pages."""
+
+    kv: torch.Tensor                      # [num_blocks, page_size, 2, D] bf16 or uint8 (e4m3)
+    block_table: torch.Tensor             # int32 [num_seqs, stride]; -1 = unmapped
+    k_scale: Optional[torch.Tensor] = None  # float32 [num_blocks * page_size] (fp8 only)
+    v_scale: Optional[torch.Tensor] = None
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kv.shape[0])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.kv.shape[1])
+
+
+@dataclass
+class Workload:
+    name: str
+    fp8: bool
+    decode: bool
+    num_heads: int
+    head_dim: int
+    window: int
+    topk: int
+    ratio: int
+    page_size: int
+    scale: float
+    q: torch.Tensor                        # bf16 [T, H, D]
+    positions: torch.Tensor                # int32 [T]
+    seq_of_token: Optional[torch.Tensor]   # int32 [T] or None (all tokens belong to sequence 0)
+    topk_idx: torch.Tensor                 # int32 [T, K]
+    win: Pool
+    cmp: Optional[Pool]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.win.block_table.shape[0])
+
+    def seq_ids(self) -> np.ndarray:
+        if self.seq_of_token is None:
+            return np.zeros(self.num_tokens, dtype=np.int64)
+        return self.seq_of_token.numpy().astype(np.int64)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw uint16 bit patterns of a bf16 tensor (numpy has no bf16 type)."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _assign_pages(g: torch.Generator, pages_per_seq: Sequence[int], oversize: int):
+    """Random physical pages for every sequence from one shared pool.
+
+    Returns (num_blocks, table[int32 B x stride]) with -1 in unused table slots.
+    """
+    total = int(sum(pages_per_seq))
+    num_blocks = max(1, total * oversize)
+    perm = torch.randperm(num_blocks, generator=g)[:total].to(torch.int32)
+    stride = max(1, max(pages_per_seq) if pages_per_seq else 1)
+    table = torch.full((len(pages_per_seq), stride), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per_seq):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    return num_blocks, table
+
+
+def _fill_pool(g: torch.Generator, num_blocks: int, page_size: int, head_dim: int,
+               referenced_pages: np.ndarray, fp8: bool, row_offset: int = 0):
+    """Pool storage: N(0,1) rows on referenced pages, NaN poison elsewhere.
+
+    ``row_offset`` extra leading rows (poisoned) model a pool that is a view into a larger
+    allocation; the returned tensors are views that start after them.
+    """
+    nrows = num_blocks * page_size
+    pages = np.nonzero(referenced_pages)[0]
+    if fp8:
+        flat = torch.full((row_offset + nrows, 2, head_dim), E4M3_NAN_CODE, dtype=torch.uint8)
+        ks = torch.full((row_offset + nrows,), float("nan"), dtype=torch.float32)
+        vs = torch.full((row_offset + nrows,), float("nan"), dtype=torch.float32)
+        kv = flat[row_offset:].view(num_blocks, page_size, 2, head_dim)
+        if len(pages):
+            x = torch.randn(len(pages), page_size, 2, head_dim, generator=g)
+            amax = x.abs().amax(dim=-1)                       # [n, ps, 2]
+            sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+            codes = (x / sc.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+            idx = torch.from_numpy(pages.astype(np.int64))
+            kv[idx] = codes.view(torch.uint8)
+            rows = (idx.view(-1, 1) * page_size + torch.arange(page_size)).reshape(-1)
+            ks[row_offset:][rows] = sc[..., 0].reshape(-1)
+            vs[row_offset:][rows] = sc[..., 1].reshape(-1)
+        return kv, ks[row_offset:], vs[row_offset:]
+    flat = torch.full((row_offset + nrows, 2, head_dim), 0, dtype=torch.int16)
+    flat.fill_(np.int16(BF16_NAN_BITS).item())
+    flat = flat.view(torch.bfloat16)
+    kv = flat[row_offset:].view(num_blocks, page_size, 2, head_dim)
+    if len(pages):
+        idx = torch.from_numpy(pages.astype(np.int64))
+        kv[idx] = torch.randn(len(pages), page_size, 2, head_dim, generator=g).to(torch.bfloat16)
+    return kv, None, None
+
+
+def build(name: str, *, seq_positions: Sequence[np.ndarray], num_heads: int, head_dim: int,
+          window: int, topk: int, ratio: int, page_size: int, fp8: bool = False, seed: int = 0,
+          oversize: int = 2, decode: bool = False, scale: Optional[float] = None,
+          cmp_entries: Optional[Sequence[int]] = None, row_offset: int = 0,
+          topk_fill: str = "sample", duplicate_topk: bool = False) -> Workload:
+    """Draw one workload.
+
+    seq_positions[b] lists the absolute positions of the queries of sequence b (queries are laid
+    out sequence after sequence).  ``cmp_entries[b]`` overrides the number of compressed entries
+    stored for sequence b (default: every entry whose tokens all lie at or before the sequence's
+    last position, i.e. ``(max_pos + 1) // ratio``).
+
+    topk_fill:
+      "sample"  - min(K, valid) distinct entries drawn uniformly from the causally valid range,
+                  random order, -1 at the tail;
+      "anywhere" - like "sample" but the -1 padding is scattered among the entries and some
+                  non-causal (future) entries are mixed in, which must be masked;
+      "empty"   - every entry -1.
+    """
+    g = torch.Generator().manual_seed(seed)
+    B = len(seq_positions)
+    pos_list = [np.asarray(p, dtype=np.int64) for p in seq_positions]
+    max_pos = [int(p.max()) for p in pos_list]
+    T = int(sum(len(p) for p in pos_list))
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+
+    # block tables
+    win_pages = [math.ceil((mp + 1) / page_size) for mp in max_pos]
+    win_blocks, win_bt = _assign_pages(g, win_pages, oversize)
+    if ratio > 0:
+        if cmp_entries is None:
+            cmp_entries = [(mp + 1) // ratio for mp in max_pos]
+        cmp_pages = [max(1, math.ceil(n / page_size)) for n in cmp_entries]
+        cmp_blocks, cmp_bt = _assign_pages(g, cmp_pages, oversize)
+    else:
+        cmp_entries = [0] * B
+
+    # queries
+    positions = torch.from_numpy(np.concatenate(pos_list).astype(np.int32))
+    seq_of_token = torch.from_numpy(
+        np.concatenate([np.full(len(p), b, dtype=np.int32) for b, p in enumerate(pos_list)]))
+    q = torch.randn(T, num_heads, head_dim, generator=g).to(torch.bfloat16)
+
+    # top-k index lists
+    topk_idx = torch.full((T, topk), -1, dtype=torch.int32)
+    if topk > 0 and ratio > 0 and topk_fill != "empty":
+        t = 0
+        for b, pl in enumerate(pos_list):
+            for p in pl:
+                valid = min(int(cmp_entries[b]), (int(p) + 1) // ratio)
+                k_eff = min(topk, valid)
+                if k_eff > 0:
+                    sel = torch.randperm(valid, generator=g)[:k_eff].to(torch.int32)
+                    if duplicate_topk and k_eff >= 2:
+                        sel[-1] = sel[0]
+                    topk_idx[t, :k_eff] = sel
+                if topk_fill == "anywhere":
+                    row = topk_idx[t].clone()
+                    future_hi = int(cmp_entries[b])
+                    if valid < future_hi:
+                        nf = min(3, topk - k_eff)
+                        fut = torch.randint(valid, future_hi, (nf,), generator=g, dtype=torch.int32)
+                        row[k_eff:k_eff + nf] = fut
+                    topk_idx[t] = row[torch.randperm(topk, generator=g)]
+                t += 1
+
+    # which physical pages any query reads
+    win_ref = np.zeros(win_blocks, dtype=bool)
+    win_bt_np = win_bt.numpy()
+    t = 0
+    for b, pl in enumerate(pos_list):
+        for p in pl:
+            lo = max(0, int(p) - window + 1) if window > 0 else int(p) + 1
+            for lp in range(lo // page_size, int(p) // page_size + 1):
+                if lo <= int(p):
+                    win_ref[win_bt_np[b, lp]] = True
+            t += 1
+    win_kv, win_ks, win_vs = _fill_pool(g, win_blocks, page_size, head_dim, win_ref, fp8,
+                                        row_offset)
+    win = Pool(win_kv, win_bt, win_ks, win_vs)
+
+    cmp = None
+    if ratio > 0:
+        cmp_ref = np.zeros(cmp_blocks, dtype=bool)
+        cmp_bt_np = cmp_bt.numpy()
+        tk = topk_idx.numpy()
+        sot = seq_of_token.numpy()
+        for t in range(T):
+            js = tk[t]
+            js = js[(js >= 0) & (js < int(cmp_entries[sot[t]]))]
+            if len(js):
+                cmp_ref[cmp_bt_np[sot[t], js // page_size]] = True
+        cmp_kv, cmp_ks, cmp_vs = _fill_pool(g, cmp_blocks, page_size, head_dim, cmp_ref, fp8,
+                                            row_offset)
+        cmp = Pool(cmp_kv, cmp_bt, cmp_ks, cmp_vs)
+
+    return Workload(name=name, fp8=fp8, decode=decode, num_heads=num_heads, head_dim=head_dim,
+                    window=window, topk=topk, ratio=ratio, page_size=page_size, scale=float(scale),
+                    q=q, positions=positions, seq_of_token=seq_of_token if (decode or B > 1) else None,
+                    topk_idx=topk_idx, win=win, cmp=cmp,
+                    meta={"seed": seed, "cmp_entries": list(cmp_entries), "oversize": oversize,
+                          "row_offset": row_offset})
+
+
+def pool_rows_referenced(w: Workload) -> int:
+    """Number of (query, column) pairs that resolve to a row: used for byte/flop accounting."""
+    total = 0
+    pos = w.positions.numpy().astype(np.int64)
+    sot = w.seq_ids()
+    tk = w.topk_idx.numpy()
+    for t in range(w.num_tokens):
+        p = int(pos[t])
+        total += min(p + 1, w.window)
+        if w.ratio > 0 and w.topk > 0:
+            js = tk[t]
+            n_ent = int(w.meta["cmp_entries"][sot[t]])
+            total += int(np.count_nonzero((js >= 0) & (w.ratio * js + w.ratio - 1 <= p)
+                                          & (js < n_ent)))
+    return total
+
+
+# Workloads named after what they are.  Sizes follow the FreeToken PR 633 "Kernel time" shapes.
+CONFIG_NAMES = (
+    "tiny_r4",              # 16 queries @ 240..255, 8 heads, D 64, window 16, top-k 32 of 64 (r 4)
+    "decode_b1_r4",         # B 1 @ 32767, 64 heads, D 512, window 128, top-k 512 of 8192 (r 4)
+    "decode_b8_r128",       # B 8 @ 32767, top-k 256 of 256 (r 128)
+    "decode_b8_r4",         # B 8 @ 32767, top-k 512 of 8192 (r 4)
+    "decode_b8_r0",         # B 8 @ 32767, window only
+    "prefill_s8192_r4",     # 8192 queries from position 0, top-k 512 (r 4)
+    "prefill_fp8_s4096_r4", # e4m3 pools, 4096 queries at 28672..32767, top-k 512 of 8192 (r 4)
+)
+
+
+def make(name: str, seed: int = 0) -> Workload:
+    """The named workloads (seed 0 unless told otherwise)."""
+    if name == "tiny_r4":
+        return build(name, seq_positions=[np.arange(240, 256)], num_heads=8, head_dim=64,
+                     window=16, topk=32, ratio=4, page_size=16, seed=seed, oversize=1)
+    if name == "decode_b1_r4":
+        return build(name, seq_positions=[np.array([32767])], num_heads=64, head_dim=512,
+                     window=128, topk=512, ratio=4, page_size=64, seed=seed, decode=True)
+    if name.startswith("decode_b8_r"):
+        r = int(name.rsplit("_r", 1)[1])
+        k = {128: 256, 4: 512, 0: 0}[r]
+        return build(name, seq_positions=[np.array([32767])] * 8, num_heads=64, head_dim=512,
+                     window=128, topk=k, ratio=r, page_size=64, seed=seed, decode=True)
+    if name == "prefill_s8192_r4":
+        return build(name, seq_positions=[np.arange(0, 8192)], num_heads=64, head_dim=512,
+                     window=128, topk=512, ratio=4, page_size=64, seed=seed)
+    if name == "prefill_fp8_s4096_r4":
+        return build(name, seq_positions=[np.arange(28672, 32768)], num_heads=64, head_dim=512,
+                     window=128, topk=512, ratio=4, page_size=64, seed=seed, fp8=True,
+                     cmp_entries=[8192])
+    raise KeyError(name)
