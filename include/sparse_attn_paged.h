@@ -1,0 +1,149 @@
+/*
+ * sparse_attn_paged.h - C ABI of the GB300 (sm_103a) sparse paged attention library.
+ *
+ * What is computed (FreeToken PR 633, "perf(kernel): keep 16-byte kv loads in dsv4 sparse
+ * attention and unroll gated pool": call paths and "Changes"; the workloads of its "Kernel time"
+ * table): every query token t, at absolute position p = positions[t] in sequence
+ * b = seq_of_token[t], attends with ONE softmax over a gathered column set:
+ *
+ *   window columns   c = 0 .. window-1  : token  x = p - window + 1 + c, present iff x >= 0,
+ *                                         row = win.block_table[b][x / ps] * ps + x % ps
+ *   top-k columns    c = window .. +topk: entry  j = topk_idx[t][c - window], present iff
+ *                                         j >= 0, ratio > 0 and ratio*j + ratio - 1 <= p,
+ *                                         row = cmp.block_table[b][j / ps] * ps + j % ps
+ *
+ *   s_c   = scale * sum_d q[t][h][d] * K[row_c][d]
+ *   out[t][h][:] = sum_c softmax(s)_c * V[row_c][:]          (bf16, round to nearest even)
+ *
+ * K/V rows have one kv_head shared by all query heads.  With fp8 pools the K and V values are
+ * e4m3 codes times a per-(token, kv_head) fp32 scale (FreeToken clone PR 3, "Perf/kv fp8 read
+ * path", part 1): the K scale multiplies the scores, the V scale multiplies the probabilities
+ * before the PV product, and the softmax denominator accumulates the unscaled probabilities.
+ *
+ * Memory layout (all device pointers are owned by the caller; the library never allocates,
+ * frees or keeps a pointer after a call returns, and never synchronises the stream except in
+ * sparse_attn_paged_check_errors):
+ *   q          bf16  [num_tokens][num_heads][head_dim], 16-byte aligned
+ *   out        bf16  [num_tokens][num_heads][head_dim], 16-byte aligned
+ *   pool.kv    [num_blocks][page_size][2][head_dim]: index 0 is K, index 1 is V; bf16, or e4m3
+ *              codes (one byte each) for the _fp8 entry points; 16-byte aligned (the pool may be
+ *              a view that starts at any row of a larger allocation)
+ *   pool.k_scale, pool.v_scale   fp32 [num_blocks * page_size] (fp8 only, else NULL)
+ *   pool.block_table             int32 [num_seqs][bt_stride]; -1 marks an unmapped page
+ *   positions  int32 [num_tokens];  seq_of_token int32 [num_tokens] or NULL (all in seq 0)
+ *   topk_idx   int32 [num_tokens][topk], -1 padded anywhere; NULL allowed when topk == 0
+ *
+ * Errors: every entry point returns an spa_status_t.  Host-side checks (NULL pointers,
+ * alignment, unsupported shapes, workspace size) return before anything is launched.  Input
+ * errors found on the device (a referenced page beyond its block table, a block id outside the
+ * pool, a sequence id outside [0, num_seqs)) drop the column and set SPA_ERR_INDEX in a device
+ * error word; a pipeline wait that exceeds its time limit sets SPA_ERR_TIMEOUT and ends the
+ * kernel early.  sparse_attn_paged_check_errors() reads and clears that word.
+ *
+ * Supported shapes: head_dim in {64, 128, ..., 512} (multiple of 64), num_heads >= 1 (heads
+ * are processed in groups of 64), window + topk <= 1024, num_blocks * page_size <= 2^30.
+ */
+#ifndef SPARSE_ATTN_PAGED_H
+#define SPARSE_ATTN_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spa_status {
+  SPA_OK = 0,
+  SPA_ERR_NULL = 1,         /* a required pointer is NULL                                      */
+  SPA_ERR_ALIGN = 2,        /* q, out, a pool or the workspace is not 16-byte aligned           */
+  SPA_ERR_SHAPE = 3,        /* negative or inconsistent sizes                                   */
+  SPA_ERR_UNSUPPORTED = 4,  /* head_dim, window + topk or pool size outside the supported range */
+  SPA_ERR_WORKSPACE = 5,    /* decode workspace smaller than sparse_attn_paged_decode_workspace_size */
+  SPA_ERR_CUDA = 6,         /* a CUDA runtime call failed: see sparse_attn_paged_last_cuda_error */
+  SPA_ERR_INDEX = 8,        /* device: a column referenced a page or block outside its table/pool */
+  SPA_ERR_TIMEOUT = 16      /* device: a pipeline wait gave up; outputs of that call are invalid */
+} spa_status_t;
+
+/* One paged pool: the window pool or the compressed pool. */
+typedef struct spa_pool {
+  const void* kv;               /* device, see layout above                                  */
+  const float* k_scale;         /* device, fp8 pools only                                    */
+  const float* v_scale;         /* device, fp8 pools only                                    */
+  const int32_t* block_table;   /* device, [num_seqs][bt_stride]                             */
+  int64_t num_blocks;           /* physical pages in the pool                                */
+  int32_t page_size;            /* rows per page (> 0)                                       */
+  int32_t bt_stride;            /* int32 entries per block-table row (> 0)                   */
+} spa_pool_t;
+
+/* Problem description shared by every entry point. */
+typedef struct spa_problem {
+  int32_t num_tokens;           /* T: query tokens (decode: one per sequence)                */
+  int32_t num_seqs;             /* B: rows of the block tables                               */
+  int32_t num_heads;            /* H: query heads sharing the single kv_head                 */
+  int32_t head_dim;             /* D                                                         */
+  int32_t window;               /* W: sliding-window columns                                 */
+  int32_t topk;                 /* K: top-k columns per query                                */
+  int32_t ratio;                /* r: compress ratio; 0 = no compressed columns (window only) */
+  float scale;                  /* softmax scale applied to q.k (e.g. 1/sqrt(head_dim))      */
+  const int32_t* positions;     /* device [T]                                                */
+  const int32_t* seq_of_token;  /* device [T] or NULL                                        */
+  const int32_t* topk_idx;      /* device [T][K] or NULL if K == 0                           */
+} spa_problem_t;
+
+/*
+ * Prefill: one pass over every column of each query (FreeToken PR 633, call paths:
+ * sparse_attn_paged -> prefill kernel).  cmp may be NULL iff ratio == 0 (the ratio-0 alias of
+ * the page's "Correctness and tests").  Asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ * default stream).  Writes out[T][H][D].
+ */
+int sparse_attn_paged_prefill(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                              const spa_problem_t* prob, void* out, void* stream);
+
+/* Same with e4m3 pools (FreeToken clone PR 3, part 1: the scale is folded into the scores and
+ * into the probabilities before PV, never into the K/V tiles). */
+int sparse_attn_paged_prefill_fp8(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                                  const spa_problem_t* prob, void* out, void* stream);
+
+/*
+ * Decode: split-K over the column set (FreeToken PR 633, call paths: the split-K decode kernel),
+ * then a log-sum-exp merge of the per-split partials into out.  The caller passes a device
+ * workspace of at least sparse_attn_paged_decode_workspace_size(prob) bytes (16-byte aligned);
+ * its contents need no initialisation and are scratch after the call.  Two calls that run
+ * concurrently must use different workspaces.
+ */
+size_t sparse_attn_paged_decode_workspace_size(const spa_problem_t* prob);
+int sparse_attn_paged_decode(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                             const spa_problem_t* prob, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                                 const spa_problem_t* prob, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Column dump (the integer half of the method, exposed for exact checks): cols[T][W + K] gets
+ * the physical row of every column, window columns as the row itself, top-k columns as
+ * (1 << 30) | row, and -1 where the column does not exist.  Uses the same device resolution
+ * code as the attention kernels.
+ */
+int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* cmp,
+                                      const spa_problem_t* prob, int32_t* cols, void* stream);
+
+/* Synchronises `stream`, returns the device error word (an OR of SPA_ERR_INDEX and
+ * SPA_ERR_TIMEOUT, 0 if clean) accumulated since the last check on the current device, and
+ * clears it.  Returns SPA_ERR_CUDA if the synchronisation itself fails. */
+int sparse_attn_paged_check_errors(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* sparse_attn_paged_strerror(int status);
+
+/* Message of the last CUDA runtime error seen by this thread (static per-thread storage). */
+const char* sparse_attn_paged_last_cuda_error(void);
+
+/* Library version string. */
+const char* sparse_attn_paged_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPARSE_ATTN_PAGED_H */

@@ -1,0 +1,245 @@
+"""GB300 (sm_103a) sparse paged attention: a thin ctypes binding over the C ABI.
+
+The C ABI is declared in ``include/sparse_attn_paged.h``; this module only marshals torch tensors
+into its plain pointers and sizes (every step of the computation runs in the library's CUDA
+kernels).  The shared library is built in-tree by ``sparse_paged_attention_gb300.build`` and is
+loaded on first use; when it is missing every call raises, there is no other code path.
+
+Pools are any object with ``kv`` ([num_blocks, page_size, 2, head_dim] bf16 or uint8 e4m3 codes),
+``block_table`` (int32 [num_seqs, stride]) and, for e4m3 pools, ``k_scale``/``v_scale`` (fp32
+[num_blocks * page_size]) attributes, e.g. :class:`PagedPool`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+__all__ = [
+    "PagedPool", "SpaError", "library_path", "load_library", "sparse_attn_paged_prefill",
+    "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8",
+    "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_resolve_columns",
+    "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
+]
+
+SPA_STATUS = {
+    "SPA_OK": 0, "SPA_ERR_NULL": 1, "SPA_ERR_ALIGN": 2, "SPA_ERR_SHAPE": 3,
+    "SPA_ERR_UNSUPPORTED": 4, "SPA_ERR_WORKSPACE": 5, "SPA_ERR_CUDA": 6, "SPA_ERR_INDEX": 8,
+    "SPA_ERR_TIMEOUT": 16,
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_lib", "libspa_gb300.so")
+
+
+class SpaPoolC(ctypes.Structure):
+    _fields_ = [("kv", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int64), ("page_size", ctypes.c_int32),
+                ("bt_stride", ctypes.c_int32)]
+
+
+class SpaProblemC(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("topk", ctypes.c_int32), ("ratio", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("positions", ctypes.c_void_p),
+                ("seq_of_token", ctypes.c_void_p), ("topk_idx", ctypes.c_void_p)]
+
+
+class SpaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load_library()
+        msg = lib.sparse_attn_paged_strerror(status).decode()
+        if status == SPA_STATUS["SPA_ERR_CUDA"]:
+            msg += ": " + lib.sparse_attn_paged_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library():
+    """Load the in-tree shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m sparse_paged_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, PP, PR = ctypes.c_void_p, ctypes.POINTER(SpaPoolC), ctypes.POINTER(SpaProblemC)
+    for name in ("sparse_attn_paged_prefill", "sparse_attn_paged_prefill_fp8"):
+        f = getattr(lib, name)
+        f.argtypes = [P, PP, PP, PR, P, P]
+        f.restype = ctypes.c_int
+    for name in ("sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8"):
+        f = getattr(lib, name)
+        f.argtypes = [P, PP, PP, PR, P, P, ctypes.c_size_t, P]
+        f.restype = ctypes.c_int
+    lib.sparse_attn_paged_decode_workspace_size.argtypes = [PR]
+    lib.sparse_attn_paged_decode_workspace_size.restype = ctypes.c_size_t
+    lib.sparse_attn_paged_resolve_columns.argtypes = [PP, PP, PR, P, P]
+    lib.sparse_attn_paged_resolve_columns.restype = ctypes.c_int
+    lib.sparse_attn_paged_check_errors.argtypes = [P]
+    lib.sparse_attn_paged_check_errors.restype = ctypes.c_int
+    lib.sparse_attn_paged_strerror.argtypes = [ctypes.c_int]
+    lib.sparse_attn_paged_strerror.restype = ctypes.c_char_p
+    lib.sparse_attn_paged_last_cuda_error.argtypes = []
+    lib.sparse_attn_paged_last_cuda_error.restype = ctypes.c_char_p
+    lib.sparse_attn_paged_version.argtypes = []
+    lib.sparse_attn_paged_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+class PagedPool(NamedTuple):
+    kv: torch.Tensor
+    block_table: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _pool_c(pool, fp8: bool) -> Optional[SpaPoolC]:
+    if pool is None:
+        return None
+    kv, bt = pool.kv, pool.block_table
+    want = torch.uint8 if fp8 else torch.bfloat16
+    if kv.dtype != want:
+        raise TypeError(f"pool kv must be {want}, got {kv.dtype}")
+    if kv.dim() != 4 or kv.shape[2] != 2 or not kv.is_contiguous():
+        raise ValueError("pool kv must be a contiguous [num_blocks, page_size, 2, head_dim] tensor")
+    if bt.dtype != torch.int32 or bt.dim() != 2 or not bt.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [num_seqs, stride] tensor")
+    ks = getattr(pool, "k_scale", None) if fp8 else None
+    vs = getattr(pool, "v_scale", None) if fp8 else None
+    return SpaPoolC(kv.data_ptr(), _ptr(ks), _ptr(vs), bt.data_ptr(), kv.shape[0], kv.shape[1],
+                    bt.shape[1])
+
+
+def _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs):
+    T, H, D = q.shape
+    K = 0 if topk_idx is None else int(topk_idx.shape[1])
+    for name, t in (("positions", positions), ("topk_idx", topk_idx), ("seq_of_token", seq_of_token)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    B = int(win.block_table.shape[0]) if num_seqs is None else int(num_seqs)
+    return SpaProblemC(T, B, H, D, int(window), K, int(ratio), float(scale), positions.data_ptr(),
+                       _ptr(seq_of_token), _ptr(topk_idx) if K > 0 else None)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_q(q):
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 [num_tokens, num_heads, head_dim] tensor")
+
+
+def _prefill(fp8, q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_of_token=None,
+             out=None, num_seqs=None, stream=None):
+    lib = load_library()
+    _check_q(q)
+    if out is None:
+        out = torch.empty_like(q)
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    w, c = _pool_c(win, fp8), _pool_c(cmp, fp8)
+    fn = lib.sparse_attn_paged_prefill_fp8 if fp8 else lib.sparse_attn_paged_prefill
+    st = fn(q.data_ptr(), ctypes.byref(w), ctypes.byref(c) if c is not None else None,
+            ctypes.byref(prob), out.data_ptr(), _stream(stream))
+    if st != 0:
+        raise SpaError(st, fn.__name__)
+    return out
+
+
+def sparse_attn_paged_prefill(q, win, cmp, topk_idx, positions, **kw):
+    """out[T, H, D] (bf16) of sparse paged attention, one pass per query (see the C header)."""
+    return _prefill(False, q, win, cmp, topk_idx, positions, **kw)
+
+
+def sparse_attn_paged_prefill_fp8(q, win, cmp, topk_idx, positions, **kw):
+    """Same with e4m3 pools (uint8 codes plus fp32 k_scale/v_scale per row)."""
+    return _prefill(True, q, win, cmp, topk_idx, positions, **kw)
+
+
+def sparse_attn_paged_decode_workspace_size(q, win, topk_idx, positions, *, window, ratio, scale,
+                                            seq_of_token=None, num_seqs=None) -> int:
+    lib = load_library()
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    return int(lib.sparse_attn_paged_decode_workspace_size(ctypes.byref(prob)))
+
+
+def _decode(fp8, q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_of_token=None,
+            out=None, workspace=None, num_seqs=None, stream=None):
+    lib = load_library()
+    _check_q(q)
+    if out is None:
+        out = torch.empty_like(q)
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    if workspace is None:
+        nbytes = int(lib.sparse_attn_paged_decode_workspace_size(ctypes.byref(prob)))
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    w, c = _pool_c(win, fp8), _pool_c(cmp, fp8)
+    fn = lib.sparse_attn_paged_decode_fp8 if fp8 else lib.sparse_attn_paged_decode
+    st = fn(q.data_ptr(), ctypes.byref(w), ctypes.byref(c) if c is not None else None,
+            ctypes.byref(prob), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != 0:
+        raise SpaError(st, fn.__name__)
+    return out
+
+
+def sparse_attn_paged_decode(q, win, cmp, topk_idx, positions, **kw):
+    """Split-K decode plus log-sum-exp merge; allocates the workspace with torch if none given."""
+    return _decode(False, q, win, cmp, topk_idx, positions, **kw)
+
+
+def sparse_attn_paged_decode_fp8(q, win, cmp, topk_idx, positions, **kw):
+    return _decode(True, q, win, cmp, topk_idx, positions, **kw)
+
+
+def sparse_attn_paged_resolve_columns(win, cmp, topk_idx, positions, *, window, ratio,
+                                      seq_of_token=None, num_seqs=None, head_dim=64,
+                                      stream=None) -> torch.Tensor:
+    """Integer column list [T, W + K]: window rows, (1 << 30) | compressed rows, -1 if absent."""
+    lib = load_library()
+    T = int(positions.shape[0])
+    K = 0 if topk_idx is None else int(topk_idx.shape[1])
+    cols = torch.full((T, window + K), -1, dtype=torch.int32, device=positions.device)
+    dummy_q = torch.empty((T, 1, head_dim), dtype=torch.bfloat16, device="meta")
+    prob = _problem_c(dummy_q, win, topk_idx, positions, seq_of_token, window, ratio, 1.0,
+                      num_seqs)
+    w = _pool_c(win, win.kv.dtype == torch.uint8)
+    c = _pool_c(cmp, cmp.kv.dtype == torch.uint8) if cmp is not None else None
+    st = lib.sparse_attn_paged_resolve_columns(ctypes.byref(w), ctypes.byref(c) if c is not None
+                                               else None, ctypes.byref(prob), cols.data_ptr(),
+                                               _stream(stream))
+    if st != 0:
+        raise SpaError(st, "sparse_attn_paged_resolve_columns")
+    return cols
+
+
+def sparse_attn_paged_check_errors(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    lib = load_library()
+    st = lib.sparse_attn_paged_check_errors(_stream(stream))
+    if st == SPA_STATUS["SPA_ERR_CUDA"]:
+        raise SpaError(st, "sparse_attn_paged_check_errors")
+    return st
+
+
+def sparse_attn_paged_strerror(status: int) -> str:
+    return load_library().sparse_attn_paged_strerror(status).decode()

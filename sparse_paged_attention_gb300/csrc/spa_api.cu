@@ -1,0 +1,271 @@
+// spa_api.cu - the C ABI: host-side validation, work planning and launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "sparse_attn_paged.h"
+#include "spa_launch.h"
+
+namespace {
+
+thread_local char g_cuda_msg[512] = "no CUDA error recorded";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return SPA_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+bool g_prepared[kMaxDevices];
+
+// SM count of the current device; sets the kernels' shared-memory attribute once per device.
+int current_device(int* dev, int* sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return SPA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_prepared[*dev]) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = spa::prepare_attn_kernels();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    g_sms[*dev] = n;
+    g_prepared[*dev] = true;
+  }
+  *sms = g_sms[*dev];
+  return SPA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_pool(const spa_pool_t* pl, bool fp8, int head_dim) {
+  if (!pl || !pl->kv || !pl->block_table) return SPA_ERR_NULL;
+  if (pl->num_blocks < 1 || pl->page_size < 1 || pl->bt_stride < 1) return SPA_ERR_SHAPE;
+  if ((long double)pl->num_blocks * pl->page_size > (long double)(1ll << 30)) return SPA_ERR_UNSUPPORTED;
+  if (!aligned16(pl->kv)) return SPA_ERR_ALIGN;
+  if (fp8 && (!pl->k_scale || !pl->v_scale)) return SPA_ERR_NULL;
+  (void)head_dim;
+  return SPA_OK;
+}
+
+bool uses_cmp(const spa_problem_t* pr) { return pr->ratio > 0 && pr->topk > 0; }
+
+int validate(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_problem_t* pr,
+             const void* out, bool fp8) {
+  if (!pr) return SPA_ERR_NULL;
+  if (pr->num_tokens < 0 || pr->num_seqs < 1 || pr->num_heads < 1 || pr->window < 0 ||
+      pr->topk < 0 || pr->ratio < 0 || pr->head_dim < 1)
+    return SPA_ERR_SHAPE;
+  if (!std::isfinite(pr->scale)) return SPA_ERR_SHAPE;
+  if (pr->head_dim % 64 != 0 || pr->head_dim > 512) return SPA_ERR_UNSUPPORTED;
+  if (pr->window + pr->topk > spa::kMaxColumns) return SPA_ERR_UNSUPPORTED;
+  if (pr->num_tokens == 0) return SPA_OK;
+  if (!q || !out || !pr->positions) return SPA_ERR_NULL;
+  if (pr->topk > 0 && !pr->topk_idx) return SPA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out)) return SPA_ERR_ALIGN;
+  int st = check_pool(win, fp8, pr->head_dim);
+  if (st) return st;
+  if (uses_cmp(pr)) {
+    st = check_pool(cmp, fp8, pr->head_dim);
+    if (st) return st;
+  }
+  return SPA_OK;
+}
+
+void fill_pool(spa::PoolDev& d, const spa_pool_t* s) {
+  d.kv = static_cast<const uint8_t*>(s->kv);
+  d.k_scale = s->k_scale;
+  d.v_scale = s->v_scale;
+  d.bt = s->block_table;
+  d.num_blocks = s->num_blocks;
+  d.ps = s->page_size;
+  d.bt_stride = s->bt_stride;
+}
+
+void fill_resolve(spa::ResolveArgs& a, const spa_pool_t* win, const spa_pool_t* cmp,
+                  const spa_problem_t* pr) {
+  std::memset(&a, 0, sizeof a);
+  fill_pool(a.win, win);
+  if (uses_cmp(pr)) {
+    fill_pool(a.cmp, cmp);
+  } else {
+    fill_pool(a.cmp, win);  // never dereferenced: ratio 0 or topk 0 yields no compressed column
+  }
+  a.positions = pr->positions;
+  a.seq_of_token = pr->seq_of_token;
+  a.topk = pr->topk_idx;
+  a.T = pr->num_tokens;
+  a.B = pr->num_seqs;
+  a.W = pr->window;
+  a.K = pr->topk;
+  a.r = uses_cmp(pr) ? pr->ratio : 0;
+}
+
+// Decode split plan: enough splits to give every SM one item, at least 32 columns per split.
+void decode_plan(const spa_problem_t* pr, int sms, int* splits, int* cols) {
+  const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
+  const long long groups = (pr->num_heads + 63) / 64;
+  const long long base = (long long)pr->num_tokens * groups;
+  long long want = base > 0 ? sms / base : 1;
+  if (want < 1) want = 1;
+  int c = (int)((C + want - 1) / want);
+  c = ((c + 31) / 32) * 32;
+  if (c > C) c = C;
+  *cols = c;
+  *splits = (C + c - 1) / c;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes(const spa_problem_t* pr, int splits) {
+  const size_t tsh = (size_t)pr->num_tokens * splits * pr->num_heads;
+  return align256(tsh * pr->head_dim * sizeof(float)) + align256(tsh * sizeof(float));
+}
+
+int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_problem_t* pr,
+        void* out, void* ws, size_t ws_bytes, void* stream, bool decode, bool fp8) {
+  int st = validate(q, win, cmp, pr, out, fp8);
+  if (st) return st;
+  if (pr->num_tokens == 0) return SPA_OK;
+  if (fp8) return SPA_ERR_UNSUPPORTED;  // e4m3 pools: not in this build yet
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st) return st;
+
+  spa::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  fill_resolve(p.rs, win, cmp, pr);
+  p.q = static_cast<const uint8_t*>(q);
+  p.out = static_cast<uint8_t*>(out);
+  p.H = pr->num_heads;
+  p.D = pr->head_dim;
+  p.n_groups = (pr->num_heads + 63) / 64;
+  p.scale_log2 = pr->scale * 1.4426950408889634f;
+  const int C = pr->window + pr->topk;
+  if (decode) {
+    int splits = 1, cols = 1;
+    decode_plan(pr, sms, &splits, &cols);
+    const size_t need = workspace_bytes(pr, splits);
+    if (!ws) return SPA_ERR_NULL;
+    if (!aligned16(ws)) return SPA_ERR_ALIGN;
+    if (ws_bytes < need) return SPA_ERR_WORKSPACE;
+    const size_t tsh = (size_t)pr->num_tokens * splits * pr->num_heads;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                        align256(tsh * pr->head_dim * sizeof(float)));
+    p.n_splits = splits;
+    p.cols_per_split = cols;
+    p.decode = 1;
+  } else {
+    p.n_splits = 1;
+    p.cols_per_split = C > 0 ? C : 1;
+    p.decode = 0;
+  }
+  const long long items = (long long)pr->num_tokens * p.n_groups * p.n_splits;
+  if (items > 0x7fffffffLL) return SPA_ERR_UNSUPPORTED;
+  p.n_items = (int)items;
+  const int grid = (int)(items < sms ? items : sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = spa::launch_attn_bf16(p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  if (decode) {
+    e = spa::launch_merge(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  }
+  return SPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_attn_paged_prefill(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                              const spa_problem_t* prob, void* out, void* stream) {
+  return run(q, win, cmp, prob, out, nullptr, 0, stream, false, false);
+}
+
+int sparse_attn_paged_prefill_fp8(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                                  const spa_problem_t* prob, void* out, void* stream) {
+  return run(q, win, cmp, prob, out, nullptr, 0, stream, false, true);
+}
+
+size_t sparse_attn_paged_decode_workspace_size(const spa_problem_t* prob) {
+  if (!prob || prob->num_tokens < 0 || prob->num_heads < 1 || prob->head_dim < 1) return 0;
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != SPA_OK) return 0;
+  int splits = 1, cols = 1;
+  decode_plan(prob, sms, &splits, &cols);
+  return workspace_bytes(prob, splits);
+}
+
+int sparse_attn_paged_decode(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                             const spa_problem_t* prob, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return run(q, win, cmp, prob, out, workspace, workspace_bytes, stream, true, false);
+}
+
+int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                                 const spa_problem_t* prob, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return run(q, win, cmp, prob, out, workspace, workspace_bytes, stream, true, true);
+}
+
+int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* cmp,
+                                      const spa_problem_t* prob, int32_t* cols, void* stream) {
+  if (!prob) return SPA_ERR_NULL;
+  if (prob->num_tokens < 0 || prob->num_seqs < 1 || prob->window < 0 || prob->topk < 0 ||
+      prob->ratio < 0)
+    return SPA_ERR_SHAPE;
+  if (prob->num_tokens == 0 || prob->window + prob->topk == 0) return SPA_OK;
+  if (!cols || !prob->positions) return SPA_ERR_NULL;
+  if (prob->topk > 0 && !prob->topk_idx) return SPA_ERR_NULL;
+  int st = check_pool(win, false, prob->head_dim);
+  if (st) return st;
+  if (uses_cmp(prob)) {
+    st = check_pool(cmp, false, prob->head_dim);
+    if (st) return st;
+  }
+  spa::ResolveArgs a;
+  fill_resolve(a, win, cmp, prob);
+  cudaError_t e = spa::launch_resolve_dump(a, cols, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "resolve kernel launch");
+  return SPA_OK;
+}
+
+int sparse_attn_paged_check_errors(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = spa::read_and_clear_error_word(&v);
+  if (e != cudaSuccess) return cuda_fail(e, "device error word");
+  return v;
+}
+
+const char* sparse_attn_paged_strerror(int status) {
+  switch (status) {
+    case SPA_OK: return "SPA_OK";
+    case SPA_ERR_NULL: return "SPA_ERR_NULL: a required pointer is NULL";
+    case SPA_ERR_ALIGN: return "SPA_ERR_ALIGN: a buffer is not 16-byte aligned";
+    case SPA_ERR_SHAPE: return "SPA_ERR_SHAPE: negative or inconsistent sizes";
+    case SPA_ERR_UNSUPPORTED: return "SPA_ERR_UNSUPPORTED: shape outside the supported range";
+    case SPA_ERR_WORKSPACE: return "SPA_ERR_WORKSPACE: decode workspace too small";
+    case SPA_ERR_CUDA: return "SPA_ERR_CUDA: CUDA runtime error";
+    case SPA_ERR_INDEX: return "SPA_ERR_INDEX: a column referenced a page or block outside its table or pool";
+    case SPA_ERR_TIMEOUT: return "SPA_ERR_TIMEOUT: a pipeline wait gave up";
+    case SPA_ERR_INDEX | SPA_ERR_TIMEOUT: return "SPA_ERR_INDEX | SPA_ERR_TIMEOUT";
+    default: return "unknown status";
+  }
+}
+
+const char* sparse_attn_paged_last_cuda_error(void) { return g_cuda_msg; }
+
+const char* sparse_attn_paged_version(void) { return "sparse_paged_attention_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

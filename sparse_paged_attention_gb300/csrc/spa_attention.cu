@@ -1,0 +1,670 @@
+// spa_attention.cu - sm_103a sparse paged attention: tcgen05 kernel, split-K merge, column dump.
+//
+// One CTA per SM runs a persistent loop over work items (query token, group of 64 heads, split
+// of the column list).  For each item it resolves and compacts the query's column set, then
+// streams it in tiles of 128 columns:
+//
+//   gather warps (5..8)  resolve columns through the block tables (FreeToken PR 633, "Changes":
+//                        per-column choice of window or compressed pool), then copy the 16-byte
+//                        pieces of every K and V row into shared memory with cp.async, already in
+//                        the 128-byte-swizzled operand layout, through a 4-slot ring.
+//   MMA warp (4)         S^T[c][h] = K[c][:] . Q[h][:]    tcgen05, M = 128 columns, N = 64 heads
+//                        O^T[d][h] += V[c][d] * P^T[c][h] tcgen05, M = 128 of head_dim, N = 64
+//                        both accumulate in TMEM (S^T double-buffered, O^T resident).
+//   softmax warps (0..3) one thread per column: read S^T from TMEM, mask, online max and sum
+//                        across columns (warp shuffles plus a 4-warp exchange), write P^T (bf16)
+//                        to shared memory; at the end divide O by the denominators and store.
+//
+// Heads sit in the N dimension, columns (and head_dim) in M = 128: an M = 128 tcgen05 tile runs
+// the tensor core at its full per-SM rate and keeps one TMEM lane per row, which a 64-row tile of
+// heads would not.
+#include <cuda_bf16.h>
+
+#include "spa_launch.h"
+
+namespace spa {
+
+namespace cfg {
+constexpr int kThreads = kAttnThreads;
+constexpr int kStages = 4;            // K/V ring slots
+constexpr int kSlotBytes = 32768;     // 128 rows x 128 head_dim values (two swizzle atoms)
+constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
+constexpr int kQAtomBytes = 8192;     // 64 heads x 128 bytes
+constexpr int kTi = 4;                // tile-info ring entries
+constexpr int kTmemCols = 512;
+constexpr int kOCol = 128;            // O^T chunks start at TMEM column 128 (S^T uses 0..127)
+constexpr float kTau = 8.0f;          // lazy rescale: keep the running max until it grows by 2^8
+
+constexpr int kRingOff = 0;
+constexpr int kQOff = kRingOff + kStages * kSlotBytes;      // 131072
+constexpr int kPOff = kQOff + 8 * kQAtomBytes;              // 196608
+constexpr int kListOff = kPOff + 128 * 128;                 // 212992
+constexpr int kRedOff = kListOff + kMaxColumns * 4;         // 217088  float [2][4][64]
+constexpr int kMrowOff = kRedOff + 2 * 4 * 64 * 4;          // 219136  float [4][64]
+constexpr int kArowOff = kMrowOff + 4 * 64 * 4;             // 220160  float [4][64]
+constexpr int kTiOff = kArowOff + 4 * 64 * 4;               // 221184  int4 [kTi]
+constexpr int kCntOff = kTiOff + kTi * 16;                  // 221248  int [8]
+constexpr int kBarOff = kCntOff + 32;                       // 221280
+
+enum {
+  B_FULL = 0, B_EMPTY = 4, B_QFULL = 8, B_QEMPTY = 9, B_SFULL = 10, B_SEMPTY = 12,
+  B_PFULL = 14, B_PVDONE = 15, B_OFREE = 16, B_TIFULL = 17, B_TIEMPTY = 21, B_RED = 25,
+  B_DRAIN = 27, B_COUNT = 28
+};
+constexpr int kMiscOff = kBarOff + B_COUNT * 8;             // TMEM base, abort flag
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;            // + slack to align the base to 1 KB
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr int kFirst = 1, kLast = 2;
+}  // namespace cfg
+
+int attn_smem_bytes() { return cfg::kSmemBytes; }
+
+// Butterfly "transpose-reduce" of 32 per-thread values across the 32 lanes of a warp: after five
+// halving steps (16 + 8 + 4 + 2 + 1 shuffles) lane L holds the reduction over the warp of value L.
+template <bool kMax>
+__device__ __forceinline__ float xreduce32(const float (&v)[32], int lane) {
+  float a[16], b[8], c[4], d[2];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float send = up ? v[k] : v[k + 16];
+      const float keep = up ? v[k + 16] : v[k];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[k] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float send = up ? a[k] : a[k + 8];
+      const float keep = up ? a[k + 8] : a[k];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 8);
+      b[k] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = up ? b[k] : b[k + 4];
+      const float keep = up ? b[k + 4] : b[k];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 4);
+      c[k] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  {
+    const bool up = lane & 2;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = up ? c[k] : c[k + 2];
+      const float keep = up ? c[k + 2] : c[k];
+      const float o = __shfl_xor_sync(0xffffffffu, send, 2);
+      d[k] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+  const bool up = lane & 1;
+  const float send = up ? d[0] : d[1];
+  const float keep = up ? d[1] : d[0];
+  const float o = __shfl_xor_sync(0xffffffffu, send, 1);
+  return kMax ? fmaxf(keep, o) : keep + o;
+}
+
+// A wait whose outcome is the same on every lane of the warp (the softmax warps shuffle right
+// after their waits, so a lane must never leave the loop alone).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// A wait that must end even when the CTA is aborting (drain before releasing TMEM).
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      flag_error(SPA_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __grid_constant__ AttnParams p) {
+  using namespace cfg;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMiscOff + 4);
+  int4* ti = reinterpret_cast<int4*>(sm + kTiOff);
+#define BAR(i) (sb + (uint32_t)kBarOff + 8u * (uint32_t)(i))
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(BAR(B_FULL + i), 128);
+      mbar_init(BAR(B_EMPTY + i), 1);
+    }
+    mbar_init(BAR(B_QFULL), 128);
+    mbar_init(BAR(B_QEMPTY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_SFULL + i), 1);
+      mbar_init(BAR(B_SEMPTY + i), 128);
+      mbar_init(BAR(B_RED + i), 4);
+    }
+    mbar_init(BAR(B_PFULL), 128);
+    mbar_init(BAR(B_PVDONE), 1);
+    mbar_init(BAR(B_OFREE), 128);
+    for (int i = 0; i < kTi; ++i) {
+      mbar_init(BAR(B_TIFULL + i), 1);
+      mbar_init(BAR(B_TIEMPTY + i), 5);
+    }
+    mbar_init(BAR(B_DRAIN), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) tmem_alloc(sb + kMiscOff, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kMiscOff);
+
+  const int D = p.D;
+  const int n_datoms = D >> 6;          // 64-wide head_dim blocks (128 bytes of bf16)
+  const int n_chunks = (D + 127) >> 7;  // 128-wide head_dim chunks (one ring slot each)
+  const int C = p.rs.W + p.rs.K;
+
+  if (warp >= 5) {
+    // ===================================== gather ======================================
+    const int ptid = threadIdx.x - 160;
+    const int pw = warp - 5;
+    int32_t* list = reinterpret_cast<int32_t*>(sm + kListOff);
+    volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);
+    const int jj = ptid & 7, r0 = ptid >> 3;
+    const size_t row_bytes = (size_t)4 * D;  // K row then V row, bf16
+    int ring = 0, tik = 0;
+    uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+      // uniform abort check: one thread samples the flag, everyone reads the copy
+      named_bar_sync(2, 128);
+      if (ptid == 0) cnt[4] = *abort_flag;
+      named_bar_sync(2, 128);
+      if (cnt[4]) break;
+      const int s = item % p.n_splits;
+      const int tg = item / p.n_splits;
+      const int g = tg % p.n_groups;
+      const int t = tg / p.n_groups;
+      const int c_lo = s * p.cols_per_split;
+      const int c_hi = min(C, c_lo + p.cols_per_split);
+      bool seq_ok;
+      const int b = seq_of(p.rs, t, &seq_ok);
+      const int pos = __ldg(p.rs.positions + t);
+      // resolve and compact the column set of this item
+      int n = 0;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 128) {
+        const int c = c0 + ptid;
+        const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t, b, pos, c) : -1;
+        const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
+        if (lane == 0) cnt[pw] = __popc(m);
+        named_bar_sync(2, 128);
+        int off = n, tot = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int cw = cnt[w];
+          off += (w < pw) ? cw : 0;
+          tot += cw;
+        }
+        if (code >= 0) list[off + __popc(m & ((1u << lane) - 1u))] = code;
+        n += tot;
+        named_bar_sync(2, 128);
+      }
+      const int n_tiles = (n + 127) >> 7;
+      const int n_ti = n_tiles > 0 ? n_tiles : 1;
+      for (int j = 0; j < n_ti; ++j) {
+        mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+        if (ptid == 0) {
+          const int nj = n == 0 ? 0 : min(128, n - j * 128);
+          const int flags = (j == 0 ? kFirst : 0) | (j == n_ti - 1 ? kLast : 0);
+          ti[tik] = make_int4(item, nj, flags, 0);
+          mbar_arrive(BAR(B_TIFULL + tik));
+        }
+        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+        if (n == 0) break;
+        if (j == 0) {
+          // Q of this token and head group -> [atom][head][128 B], heads beyond H zero-filled
+          mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
+          q_ph ^= 1;
+          const uint32_t qs = sb + kQOff;
+          for (int it = 0; it < 4 * n_datoms; ++it) {
+            const int h = (it & 3) * 16 + r0;
+            const int a = it >> 2;
+            const int hg = g * 64 + h;
+            const bool ok = hg < p.H;
+            const uint8_t* src = p.q + (((size_t)t * p.H + (ok ? hg : 0)) * D) * 2 + a * 128 + jj * 16;
+            cp_async_16(qs + a * kQAtomBytes + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(BAR(B_QFULL));
+        }
+        // the 8 rows of this tile that this thread copies
+        const uint8_t* src[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int idx = j * 128 + k * 16 + r0;
+          const int32_t code = idx < n ? list[idx] : -1;
+          if (code < 0) {
+            src[k] = nullptr;
+          } else {
+            const uint8_t* base = (code >> kColPoolShift) ? p.rs.cmp.kv : p.rs.win.kv;
+            src[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
+          }
+        }
+        for (int half = 0; half < 2; ++half) {      // K rows, then V rows
+          for (int kc = 0; kc < n_chunks; ++kc) {
+            mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
+            const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int r = k * 16 + r0;
+#pragma unroll
+              for (int aa = 0; aa < 2; ++aa) {
+                const int atom = 2 * kc + aa;
+                if (atom < n_datoms) {
+                  const uint8_t* sp = src[k] ? src[k] + half * (2 * D) + atom * 128 + jj * 16 : p.q;
+                  cp_async_16(slot + aa * kAtomBytes + r * 128 + ((jj ^ (r & 7)) << 4), sp,
+                              src[k] ? 16u : 0u);
+                }
+              }
+            }
+            cp_async_arrive_noinc(BAR(B_FULL + ring));
+            if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+          }
+        }
+      }
+    }
+    // end-of-work marker for the consumers
+    if (!*abort_flag) {
+      mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+      if (ptid == 0) {
+        ti[tik] = make_int4(-1, 0, kFirst | kLast, 0);
+        mbar_arrive(BAR(B_TIFULL + tik));
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 4) {
+    // ====================================== MMA ========================================
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(128, 64, 0, 0);  // A = K rows (K-major), B = Q (K-major)
+      const uint32_t idO = idesc_bf16(128, 64, 1, 1);  // A = V^T (MN-major), B = P^T (MN-major)
+      const uint32_t qbase = sb + kQOff, pbase = sb + kPOff;
+      int ring = 0, tik = 0, sbuf = 0;
+      uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
+      for (;;) {
+        if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
+        const int4 e = ti[tik];
+        mbar_arrive(BAR(B_TIEMPTY + tik));
+        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+        if (e.x < 0) break;
+        const int n = e.y;
+        if (n == 0) continue;
+        const bool first = e.z & kFirst, last = e.z & kLast;
+        if (first) {
+          if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;
+          q_ph ^= 1;
+        }
+        if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) break;
+        s_ph ^= 1u << sbuf;
+        tc_fence_after();
+        bool ok = true;
+        const uint32_t dS = tmem + sbuf * 64;
+        for (int kc = 0; kc < n_chunks; ++kc) {
+          if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+          for (int aa = 0; aa < 2; ++aa) {
+            const int atom = 2 * kc + aa;
+            if (atom >= n_datoms) break;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t da = sdesc(slot + aa * kAtomBytes + ks * 32, 16, 1024);
+              const uint64_t db = sdesc(qbase + atom * kQAtomBytes + ks * 32, 16, 1024);
+              mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
+            }
+          }
+          mma_commit(BAR(B_EMPTY + ring));
+          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(BAR(B_SFULL + sbuf));
+        if (last) mma_commit(BAR(B_QEMPTY));
+        sbuf ^= 1;
+        if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) break;
+        p_ph ^= 1;
+        if (first) {
+          if (!mbar_wait(BAR(B_OFREE), o_ph ^ 1, abort_flag)) break;
+          o_ph ^= 1;
+        }
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const int nk = (n + 15) >> 4;
+        for (int vc = 0; vc < n_chunks; ++vc) {
+          if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+          const uint32_t dO = tmem + kOCol + vc * 64;
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t da = sdesc(slot + kk * 2048, kAtomBytes, 1024);
+            const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+            mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(BAR(B_EMPTY + ring));
+          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(BAR(B_PVDONE));
+      }
+      // nothing may still write TMEM when it is released
+      mma_commit(BAR(B_DRAIN));
+      mbar_wait_drain(BAR(B_DRAIN), 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================ softmax / epilogue ================================
+    const int tid = threadIdx.x;  // column of the tile == TMEM lane
+    float* red = reinterpret_cast<float*>(sm + kRedOff);
+    float* mrow = reinterpret_cast<float*>(sm + kMrowOff) + warp * 64;
+    float* arow = reinterpret_cast<float*>(sm + kArowOff) + warp * 64;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    int tik = 0, sbuf = 0, rb = 0;
+    uint32_t ti_ph = 0, s_ph = 0, pv_ph = 0, red_ph = 0;
+    // running max (base-2 units) and this warp's partial denominator of heads 2*lane, 2*lane+1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int t = 0, g = 0, s = 0;
+    bool had = false;
+    for (;;) {
+      if (!warp_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
+      const int4 e = ti[tik];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_TIEMPTY + tik));
+      if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+      if (e.x < 0) break;
+      const int n = e.y;
+      const bool first = e.z & kFirst, last = e.z & kLast;
+      if (first) {
+        s = e.x % p.n_splits;
+        const int tg = e.x / p.n_splits;
+        g = tg % p.n_groups;
+        t = tg / p.n_groups;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+        had = false;
+      }
+      if (n > 0) {
+        had = true;
+        if (!warp_wait(BAR(B_SFULL + sbuf), (s_ph >> sbuf) & 1u, abort_flag)) break;
+        s_ph ^= 1u << sbuf;
+        tc_fence_after();
+        const bool valid = tid < n;
+        const uint32_t s_addr = lane_base + sbuf * 64;
+        float* rr = red + rb * 256;
+        // pass 1: tile maximum of every head (lane L ends up with heads L and 32 + L)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          tmem_ld32(s_addr + hf * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = valid ? x[k] * sl2 : -INFINITY;
+          rr[warp * 64 + hf * 32 + lane] = xreduce32<true>(x, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_RED + rb));
+        if (!warp_wait(BAR(B_RED + rb), (red_ph >> rb) & 1u, abort_flag)) break;
+        red_ph ^= 1u << rb;
+        float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          M0 = fmaxf(M0, rr[w * 64 + lane]);
+          M1 = fmaxf(M1, rr[w * 64 + 32 + lane]);
+        }
+        rb ^= 1;
+        const float n0 = (M0 > m0 + kTau) ? M0 : m0;
+        const float n1 = (M1 > m1 + kTau) ? M1 : m1;
+        const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
+        const bool grow = __any_sync(0xffffffffu, (n0 != m0) || (n1 != m1));
+        m0 = n0;
+        m1 = n1;
+        mrow[lane] = n0;
+        mrow[32 + lane] = n1;
+        arow[lane] = a0;
+        arow[32 + lane] = a1;
+        __syncwarp();
+        if (grow && !first) {
+          // the running max moved: rescale O (its last PV finished before this S was ready)
+          for (int i = 0; i < n_chunks; ++i) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              float o[32];
+              const uint32_t ta = lane_base + kOCol + i * 64 + hf * 32;
+              tmem_ld32(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] *= arow[hf * 32 + k];
+              tmem_st32(ta, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        l0 *= a0;
+        l1 *= a1;
+        if (!first) {
+          // P buffer reuse: the previous PV of this item is complete
+          if (!warp_wait(BAR(B_PVDONE), pv_ph, abort_flag)) break;
+          pv_ph ^= 1;
+        }
+        // pass 2: probabilities, P^T row of this column (bf16), this warp's denominators
+        uint8_t* prow = sm + kPOff + tid * 128;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          tmem_ld32(s_addr + hf * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            x[k] = valid ? fast_exp2(x[k] * sl2 - mrow[hf * 32 + k]) : 0.f;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int k = hf * 4 + q4;  // 16-byte chunk: heads 8k .. 8k+7
+            uint4 u;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(x[8 * q4 + 0], x[8 * q4 + 1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(x[8 * q4 + 2], x[8 * q4 + 3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q4 + 4], x[8 * q4 + 5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(x[8 * q4 + 6], x[8 * q4 + 7]);
+            u.x = *reinterpret_cast<uint32_t*>(&b0);
+            u.y = *reinterpret_cast<uint32_t*>(&b1);
+            u.z = *reinterpret_cast<uint32_t*>(&b2);
+            u.w = *reinterpret_cast<uint32_t*>(&b3);
+            *reinterpret_cast<uint4*>(prow + ((k ^ (tid & 7)) << 4)) = u;
+          }
+          const float ts = xreduce32<false>(x, lane);
+          if (hf == 0) l0 += ts; else l1 += ts;
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_SEMPTY + sbuf));
+        sbuf ^= 1;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(BAR(B_PFULL));
+      }
+      if (last) {
+        const int Hg = min(64, p.H - g * 64);
+        if (!had) {
+          // no column at all: out = 0 (prefill) or an empty partial (decode)
+          if (p.decode) {
+            const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * 64;
+            for (int i = tid; i < Hg * D; i += 128) p.ws_o[pb * D + i] = 0.f;
+            if (tid < Hg) p.ws_lse[pb + tid] = -INFINITY;
+          } else {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)t * p.H + g * 64) * D;
+            for (int i = tid; i < Hg * D; i += 128) o[i] = __float2bfloat16_rn(0.f);
+          }
+          continue;
+        }
+        if (!warp_wait(BAR(B_PVDONE), pv_ph, abort_flag)) break;
+        pv_ph ^= 1;
+        tc_fence_after();
+        // softmax denominators per head
+        float* rr = red + rb * 256;
+        rr[warp * 64 + lane] = l0;
+        rr[warp * 64 + 32 + lane] = l1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_RED + rb));
+        if (!warp_wait(BAR(B_RED + rb), (red_ph >> rb) & 1u, abort_flag)) break;
+        red_ph ^= 1u << rb;
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          L0 += rr[w * 64 + lane];
+          L1 += rr[w * 64 + 32 + lane];
+        }
+        rb ^= 1;
+        arow[lane] = 1.f / L0;
+        arow[32 + lane] = 1.f / L1;
+        __syncwarp();
+        if (p.decode && warp == 0) {
+          const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * 64;
+          if (lane < Hg) p.ws_lse[pb + lane] = m0 + __log2f(L0);
+          if (32 + lane < Hg) p.ws_lse[pb + 32 + lane] = m1 + __log2f(L1);
+        }
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float inv[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) inv[k] = arow[hf * 32 + k];
+          const size_t row0 = (size_t)t * p.H + g * 64 + hf * 32;  // first head of this half
+          const int nh = min(32, Hg - hf * 32);                     // heads of this half present
+#pragma unroll 1
+          for (int i = 0; i < n_chunks; ++i) {
+            const int d = i * 128 + tid;
+            float o[32];
+            tmem_ld32(lane_base + kOCol + i * 64 + hf * 32, o);
+            tmem_wait_ld();
+            if (d < D) {
+              if (p.decode) {
+                float* wo = p.ws_o + (((size_t)t * p.n_splits + s) * p.H + g * 64 + hf * 32) * D + d;
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                  if (k < nh) wo[(uint32_t)(k * D)] = o[k] * inv[k];
+              } else {
+                // lanes 2m and 2m+1 swap halves so each stores two adjacent head_dim values
+                const bool odd = lane & 1;
+                __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) + row0 * D + (d & ~1);
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                  const float v0 = o[k] * inv[k], v1 = o[k + 1] * inv[k + 1];
+                  const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                  const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(recv, v1)
+                                                : __floats2bfloat162_rn(v0, recv);
+                  const int hh = k + (odd ? 1 : 0);
+                  if (hh < nh) *reinterpret_cast<__nv_bfloat162*>(ob + (uint32_t)(hh * D)) = pr;
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_OFREE));
+      }
+    }
+  }
+#undef BAR
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Log-sum-exp merge of the split partials (base-2 LSE): out = sum_s 2^(lse_s - L) O_s / sum_s
+// 2^(lse_s - L), L = max_s lse_s.  One block per (token, head).
+__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws_o,
+                                                    const float* __restrict__ ws_lse,
+                                                    __nv_bfloat16* __restrict__ out, int S, int H,
+                                                    int D) {
+  const int t = blockIdx.x / H, h = blockIdx.x % H;
+  const float* lse = ws_lse + (size_t)t * S * H + h;
+  float L = -INFINITY;
+  for (int s = 0; s < S; ++s) L = fmaxf(L, lse[(size_t)s * H]);
+  for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (L > -INFINITY) {
+      for (int s = 0; s < S; ++s) {
+        const float l = lse[(size_t)s * H];
+        if (l == -INFINITY) continue;
+        const float w = exp2f(l - L);
+        const float4 o = *reinterpret_cast<const float4*>(ws_o + (((size_t)t * S + s) * H + h) * D + d);
+        wsum += w;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + ((size_t)t * H + h) * D + d) = u;
+  }
+}
+
+__global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ cols) {
+  const int C = a.W + a.K;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)a.T * C) return;
+  const int t = (int)(i / C), c = (int)(i % C);
+  bool ok;
+  const int b = seq_of(a, t, &ok);
+  cols[i] = ok ? resolve_column(a, t, b, __ldg(a.positions + t), c) : -1;
+}
+
+cudaError_t prepare_attn_kernels() {
+  return cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              cfg::kSmemBytes);
+}
+
+cudaError_t launch_attn_bf16(const AttnParams& p, int grid, cudaStream_t stream) {
+  attn_bf16_kernel<<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream) {
+  merge_kernel<<<p.rs.T * p.H, 128, 0, stream>>>(p.ws_o, p.ws_lse,
+                                                 reinterpret_cast<__nv_bfloat16*>(p.out),
+                                                 p.n_splits, p.H, p.D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_resolve_dump(const ResolveArgs& a, int32_t* cols, cudaStream_t stream) {
+  const long long total = (long long)a.T * (a.W + a.K);
+  if (total == 0) return cudaSuccess;
+  const int blocks = (int)((total + 255) / 256);
+  resolve_dump_kernel<<<blocks, 256, 0, stream>>>(a, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_error_word(int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_spa_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_spa_error, &zero, sizeof(int));
+}
+
+}  // namespace spa

@@ -1,0 +1,36 @@
+// spa_launch.h - parameters and launchers shared by the kernel file and the C ABI file.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spa_device.cuh"
+
+namespace spa {
+
+struct AttnParams {
+  ResolveArgs rs;
+  const uint8_t* q;     // bf16 [T][H][D]
+  uint8_t* out;         // bf16 [T][H][D] (prefill)
+  float* ws_o;          // decode partials [T][S][H][D], each normalised by its own denominator
+  float* ws_lse;        // decode partial log-sum-exp, base 2, [T][S][H]
+  int H, D;
+  int n_groups;         // ceil(H / 64): heads are processed 64 at a time
+  int n_splits;         // S: split-K parts per (token, head group); 1 for prefill
+  int cols_per_split;   // raw columns per split
+  int n_items;          // T * n_groups * n_splits
+  float scale_log2;     // softmax scale * log2(e)
+  int decode;
+};
+
+// Kernel launch configuration.
+constexpr int kAttnThreads = 288;     // 4 softmax warps + 1 MMA warp + 4 gather warps
+int attn_smem_bytes();
+constexpr int kMaxColumns = 1024;     // window + top-k columns per query
+
+cudaError_t launch_attn_bf16(const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_resolve_dump(const ResolveArgs& a, int32_t* cols, cudaStream_t stream);
+cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)
+cudaError_t read_and_clear_error_word(int* value);
+
+}  // namespace spa

@@ -1,0 +1,94 @@
+"""The C ABI library: builds for sm_103a, loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import sparse_paged_attention_gb300 as spa
+from sparse_paged_attention_gb300 import SpaPoolC, SpaProblemC
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(spa.library_path()):
+        from sparse_paged_attention_gb300.build import build_library
+        build_library()
+    return spa.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(sparse_attn_paged_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("sparse_attn_paged_prefill", "sparse_attn_paged_decode",
+                 "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode_fp8",
+                 "sparse_attn_paged_resolve_columns", "sparse_attn_paged_check_errors"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_and_version(lib):
+    for code, name in [(0, "SPA_OK"), (1, "SPA_ERR_NULL"), (2, "SPA_ERR_ALIGN"),
+                       (4, "SPA_ERR_UNSUPPORTED"), (8, "SPA_ERR_INDEX"), (16, "SPA_ERR_TIMEOUT")]:
+        assert spa.sparse_attn_paged_strerror(code).startswith(name)
+    assert b"sm_103a" in lib.sparse_attn_paged_version()
+
+
+def _args(D=512, W=128, K=512, ratio=4, T=1, kv=0x1000, q=0x2000, out=0x3000):
+    pool = SpaPoolC(kv, None, None, 0x4000, 64, 64, 16)
+    cpool = SpaPoolC(kv, None, None, 0x5000, 64, 64, 16)
+    prob = SpaProblemC(T, 1, 64, D, W, K, ratio, 0.04, 0x6000, None, 0x7000)
+    return pool, cpool, prob, q, out
+
+
+def _prefill(lib, pool, cpool, prob, q, out):
+    return lib.sparse_attn_paged_prefill(q, ctypes.byref(pool),
+                                         ctypes.byref(cpool) if cpool is not None else None,
+                                         ctypes.byref(prob) if prob is not None else None, out,
+                                         None)
+
+
+def test_host_validation(lib):
+    S = spa.SPA_STATUS
+    pool, cpool, prob, q, out = _args()
+    assert _prefill(lib, pool, cpool, None, q, out) == S["SPA_ERR_NULL"]
+    assert _prefill(lib, pool, cpool, prob, None, out) == S["SPA_ERR_NULL"]
+    assert _prefill(lib, pool, cpool, prob, q + 2, out) == S["SPA_ERR_ALIGN"]
+    assert _prefill(lib, pool, cpool, prob, q, out + 8) == S["SPA_ERR_ALIGN"]
+    p2, c2, *_ = _args(kv=0x1002)
+    assert _prefill(lib, p2, c2, prob, q, out) == S["SPA_ERR_ALIGN"]
+    assert _prefill(lib, pool, None, prob, q, out) == S["SPA_ERR_NULL"]       # ratio > 0 needs cmp
+    for D in (32, 96, 576, 1024):
+        _, _, pr, *_ = _args(D=D)
+        assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_UNSUPPORTED"]
+    _, _, pr, *_ = _args(W=600, K=600)
+    assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_UNSUPPORTED"]
+    _, _, pr, *_ = _args(W=-1)
+    assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_SHAPE"]
+    _, _, pr, *_ = _args(T=0)
+    assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_OK"]             # nothing to do
+    big = SpaPoolC(0x1000, None, None, 0x4000, 1 << 25, 64, 16)
+    assert _prefill(lib, big, cpool, prob, q, out) == S["SPA_ERR_UNSUPPORTED"]
+    # fp8 pools need their scales
+    assert lib.sparse_attn_paged_prefill_fp8(q, ctypes.byref(pool), ctypes.byref(cpool),
+                                             ctypes.byref(prob), out, None) == S["SPA_ERR_NULL"]
+    # decode: workspace checks come before any launch
+    assert lib.sparse_attn_paged_decode(q, ctypes.byref(pool), ctypes.byref(cpool),
+                                        ctypes.byref(prob), out, None, 0, None) in (
+        S["SPA_ERR_NULL"], S["SPA_ERR_CUDA"])
