@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 sparse paged attention hot path.
+
+Headline: one decode call of the B=1 workload at position 32767 (64 heads, head_dim 512, window 128,
+top-k 512 of 8192 compressed entries, ratio 4, page size 64; the shape of the FreeToken PR 633
+"Kernel time" table), in microseconds per call, L2 flushed between calls.  The same JSON line
+carries the other workloads of the table (decode B=8 at ratios 128/4/0, prefill S=8192, the e4m3
+prefill chunk) with their achieved GB/s or TFLOP/s against the measured GB300 peaks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+For N > 1 (torchrun, one rank per GPU) every rank runs the same workload on its own GPU (the
+problem shards into independent queries/sequences; there is no data-path collective): the
+reported time is the maximum over ranks and scaling is weak.  ``--impl reference`` times the
+float64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse attn µs/call; decode HBM GB/s and prefill TFLOP/s as % of GB300 peak"
+HEADLINE = "decode_b1_r4"
+SUB_WORKLOADS = ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0", "prefill_s8192_r4",
+                 "prefill_fp8_s4096_r4"]
+FLUSH_BYTES = 512 << 20   # > 129 MB of L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed plumbing (timing only: barriers and a max over ranks, never on the data path)
+# ----------------------------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------
+# accounting
+# ----------------------------------------------------------------------------------------------
+def algorithmic_work(w):
+    """Bytes the method must move and flops it must do for one call (the dense attention it
+    avoids is not counted): every resolved K and V row once, q in, out, the index lists."""
+    from workloads import pool_rows_referenced
+    cols = pool_rows_referenced(w)
+    elt = 1 if w.fp8 else 2
+    row_bytes = 2 * w.head_dim * elt + (8 if w.fp8 else 0)   # K row + V row (+ two fp32 scales)
+    T, H, D = w.q.shape
+    nbytes = cols * row_bytes + 2 * T * H * D * 2 + T * (w.topk + 1) * 4
+    flops = 4.0 * H * D * cols
+    return {"columns": cols, "bytes": nbytes, "flops": flops}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_paged_attention_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                    + glob.glob(os.path.join(csrc, "*.h"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks sampled while the GPU is busy
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        busy = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+class Runner:
+    """One workload resident on the GPU plus the call that computes it through the C ABI."""
+
+    def __init__(self, name, device):
+        import torch
+        import sparse_paged_attention_gb300 as spa
+        from workloads import make
+        self.spa = spa
+        self.w = w = make(name)
+        g = lambda t: None if t is None else t.to(device)
+        self.q, self.pos = g(w.q), g(w.positions)
+        self.tk = g(w.topk_idx) if w.topk > 0 else None
+        self.sot = g(w.seq_of_token)
+        self.win = spa.PagedPool(g(w.win.kv), g(w.win.block_table), g(w.win.k_scale),
+                                 g(w.win.v_scale))
+        self.cmp = None if w.cmp is None else spa.PagedPool(
+            g(w.cmp.kv), g(w.cmp.block_table), g(w.cmp.k_scale), g(w.cmp.v_scale))
+        self.out = torch.empty_like(self.q)
+        self.kw = dict(window=w.window, ratio=w.ratio, scale=w.scale, seq_of_token=self.sot)
+        if w.decode:
+            n = spa.sparse_attn_paged_decode_workspace_size(self.q, self.win, self.tk, self.pos,
+                                                            **self.kw)
+            self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+            self.fn = spa.sparse_attn_paged_decode_fp8 if w.fp8 else spa.sparse_attn_paged_decode
+            self.launches_per_call = 2
+        else:
+            self.ws = None
+            self.fn = spa.sparse_attn_paged_prefill_fp8 if w.fp8 else spa.sparse_attn_paged_prefill
+            self.launches_per_call = 1
+
+    def call(self, q=None, tk=None, pos=None, out=None):
+        kw = dict(self.kw, out=self.out if out is None else out)
+        if self.ws is not None:
+            kw["workspace"] = self.ws
+        return self.fn(self.q if q is None else q, self.win, self.cmp,
+                       self.tk if tk is None else tk, self.pos if pos is None else pos, **kw)
+
+
+def time_device(fn, steps, warmup, flush, dist=None):
+    """Per-call device time (ms) of `steps` calls, L2 flushed before each (outside the events)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_e2e(r, steps, warmup, flush):
+    """The same call with host inputs: pinned host -> device copy of q, top-k and positions,
+    the call, device -> host copy of out, all inside the timed region."""
+    import torch
+    q_h = r.w.q.pin_memory()
+    pos_h = r.w.positions.pin_memory()
+    tk_h = r.w.topk_idx.pin_memory() if r.tk is not None else None
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype, pin_memory=True)
+    q_d, pos_d = torch.empty_like(r.q), torch.empty_like(r.pos)
+    tk_d = torch.empty_like(r.tk) if r.tk is not None else None
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        if tk_d is not None:
+            tk_d.copy_(tk_h, non_blocking=True)
+        r.call(q=q_d, tk=tk_d, pos=pos_d)
+        out_h.copy_(r.out, non_blocking=True)
+
+    times = time_device(step, steps, warmup, flush)
+    h2d = q_h.numel() * 2 + pos_h.numel() * 4 + (tk_h.numel() * 4 if tk_h is not None else 0)
+    d2h = out_h.numel() * 2
+    return times, h2d, d2h
+
+
+def measure_workload(name, device, steps, warmup, flush, peaks):
+    import torch
+    r = Runner(name, device)
+    r.call()
+    torch.cuda.synchronize()
+    st = r.spa.sparse_attn_paged_check_errors()
+    if st:
+        raise RuntimeError(f"{name}: device error word {st}")
+    times = time_device(r.call, steps, warmup, flush)
+    us = 1e3 * statistics.mean(times)
+    work = algorithmic_work(r.w)
+    d = {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
+         "calls": steps, "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"]}
+    if r.w.decode:
+        gbs = work["bytes"] / (us * 1e-6) / 1e9
+        d.update(bound="hbm", achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm_gbs"],
+                 frac=round(gbs / peaks["hbm_gbs"], 4))
+    else:
+        tf = work["flops"] / (us * 1e-6) / 1e12
+        peak = peaks["bf16_tflops_sustained"] * (2.0 if r.w.fp8 else 1.0)
+        d.update(bound="tensor", achieved=round(tf, 1), unit="TFLOP/s", peak=peak,
+                 frac=round(tf / peak, 4), frac_of_bf16_peak=round(tf / peaks["bf16_tflops"], 4))
+    del r
+    torch.cuda.empty_cache()
+    return d
+
+
+def cpu_baseline(name, seconds):
+    """The float64 oracle as it stands, on the host cores, in a fresh process."""
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_timing(%r, %f)))" % (ROOT, name, seconds))
+    try:
+        p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                           timeout=600)
+        return json.loads(p.stdout.strip().splitlines()[-1])
+    except Exception as e:  # noqa: BLE001 - reported, never fatal to the GPU numbers
+        return {"error": str(e)[:200]}
+
+
+def oracle_timing(name, seconds):
+    """Time the oracle on up to `seconds` of work for workload `name` (per call = all its
+    queries; prefill workloads are sampled query by query and scaled to a full call)."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_io import oracle_args
+    import oracle
+    from workloads import make
+    w = make(name)
+    a = oracle_args(w)
+    T = w.num_tokens
+    rng = np.random.default_rng(0)
+    done, t0 = 0, time.perf_counter()
+    queries = 0
+    while time.perf_counter() - t0 < seconds:
+        toks = rng.choice(T, size=min(T, 8), replace=False) if T > 8 else None
+        oracle.sparse_paged_attention(**a, tokens=toks)
+        queries += T if toks is None else len(toks)
+        done += 1
+    el = time.perf_counter() - t0
+    per_query = el / queries
+    return {"us_per_call": per_query * T * 1e6, "queries": int(queries), "seconds": round(el, 2),
+            "cores": os.cpu_count(), "per_call_queries": T}
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    peaks, peak_src = load_peaks()
+    import sparse_paged_attention_gb300 as spa
+    spa.load_library()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    with ClockSampler(local) as clk:
+        r = Runner(HEADLINE, device)
+        times = time_device(r.call, args.steps, args.warmup, flush, dist)
+        st = spa.sparse_attn_paged_check_errors()
+        if st:
+            raise RuntimeError(f"device error word {st}")
+        us = 1e3 * statistics.mean(times)
+        us_max = max_over_ranks(dist, us, device)
+        e2e_times, h2d, d2h = time_e2e(r, args.steps, args.warmup, flush)
+        e2e_us = max_over_ranks(dist, 1e3 * statistics.mean(e2e_times), device)
+        launches = r.launches_per_call * args.steps
+        work = algorithmic_work(r.w)
+        del r
+        sub = {}
+        if not args.no_sub:
+            for name in SUB_WORKLOADS:
+                try:
+                    n = 50 if name.startswith("decode") else 10
+                    sub[name] = measure_workload(name, device, n, 3, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - an unfinished path is reported, not fatal
+                    sub[name] = {"error": str(e)[:300]}
+        # keep the GPU busy long enough for the clock sampler to see it under load
+        r = Runner(HEADLINE, device)
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(200):
+                r.call()
+            torch.cuda.synchronize()
+        del r
+    clocks = clk.summary()
+
+    if rank != 0:
+        return
+    achieved = work["bytes"] / (us_max * 1e-6) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(us_max, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_max / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rows, random block tables and top-k; no dataset)",
+        "config": {"workload": "decode B=1 at position 32767, 64 heads, head_dim 512, window 128, "
+                               "top-k 512 of 8192 (ratio 4), page size 64, bf16 pools",
+                   "l2": f"flushed before every call ({FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": ncu_traffic("attn_bf16_kernel", HEADLINE),
+                     "peak_source": peak_src,
+                     "note": "algorithmic bytes / device time of the whole call (split kernel + merge)"},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "workloads": sub,
+    }
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline(HEADLINE, args.cpu_seconds)
+        if "us_per_call" in cb:
+            line["cpu_baseline"] = {"value": round(cb["us_per_call"], 1), "unit": "us/call",
+                                    "cores": cb["cores"], "kind": "oracle",
+                                    "sample": f"{cb['queries']} decode calls of the same workload "
+                                              f"in {cb['seconds']} s, float64 numpy, BLAS threads "
+                                              f"at the library default"}
+        else:
+            line["cpu_baseline"] = {"value": None, "kind": "oracle", "error": cb.get("error")}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_io import oracle_args
+    import oracle
+    from workloads import make
+    w = make(HEADLINE)
+    a = oracle_args(w)
+    for _ in range(args.warmup):
+        oracle.sparse_paged_attention(**a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sparse_paged_attention(**a)
+    el = time.perf_counter() - t0
+    us = el / args.steps * 1e6
+    line = {
+        "metric": METRIC, "value": round(us, 1), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) rows, random block tables and top-k; no dataset)",
+        "config": {"workload": "decode B=1 at position 32767, 64 heads, head_dim 512, window 128, "
+                               "top-k 512 of 8192 (ratio 4), page size 64, bf16 pools"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{args.steps} full decode calls, float64 numpy oracle"},
+        "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-sub", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,8 +1,8 @@
 """CUDA path against the float64 oracle, element by element, through the C ABI (needs a GPU).
 
 Tolerances on bf16 outputs: max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3 (the
-contract), plus a tighter regression gate on the mean for the bf16 pools.  The column list must
-match exactly.
+contract), plus a tighter regression gate for bf16 pools: mean |gpu - oracle| <= 1% of mean |oracle|
+(rounding the output to bf16 alone costs about 0.15%).  The column list must match exactly.
 """
 import numpy as np
 import pytest
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
-MEAN_ABS_BF16_GATE = 5e-4
+REL_MEAN_GATE_BF16 = 1e-2
 
 
 def _dev():
@@ -69,7 +69,9 @@ def compare(out, ref, tokens=None, gate=None, what=""):
     assert mx <= MAX_ABS, (what, mx)
     assert mean <= MEAN_ABS, (what, mean)
     if gate is not None:
-        assert mean <= gate, (what, mean, gate)
+        rel = mean / float(np.abs(ref).mean())
+        print(f"{what}: mean abs / mean |ref| = {rel:.2e}")
+        assert rel <= gate, (what, rel, gate)
     return mx, mean
 
 
@@ -95,8 +97,8 @@ def test_column_dump_exact(name):
 def test_tiny_prefill_and_decode():
     d = OnDevice(make("tiny_r4"), _dev())
     ref, _, _, _ = run_oracle(d.w)
-    compare(d.prefill(), ref, gate=MEAN_ABS_BF16_GATE, what="tiny prefill")
-    compare(d.decode(), ref, gate=MEAN_ABS_BF16_GATE, what="tiny decode")
+    compare(d.prefill(), ref, gate=REL_MEAN_GATE_BF16, what="tiny prefill")
+    compare(d.decode(), ref, gate=REL_MEAN_GATE_BF16, what="tiny decode")
     check_no_device_error()
 
 
@@ -104,8 +106,8 @@ def test_tiny_prefill_and_decode():
 def test_decode_workloads(name):
     d = OnDevice(make(name), _dev())
     ref, _, _, _ = run_oracle(d.w)
-    compare(d.decode(), ref, gate=MEAN_ABS_BF16_GATE, what=f"{name} decode")
-    compare(d.prefill(), ref, gate=MEAN_ABS_BF16_GATE, what=f"{name} via prefill")
+    compare(d.decode(), ref, gate=REL_MEAN_GATE_BF16, what=f"{name} decode")
+    compare(d.prefill(), ref, gate=REL_MEAN_GATE_BF16, what=f"{name} via prefill")
     check_no_device_error()
 
 
@@ -123,7 +125,7 @@ def test_prefill_s8192_sampled():
     check_no_device_error()
     toks = _sample_tokens(d.w.num_tokens, 50, 1)
     ref, _, _, _ = run_oracle(d.w, tokens=toks)
-    compare(out, ref, tokens=toks, gate=MEAN_ABS_BF16_GATE, what="prefill S8192 (sampled)")
+    compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_BF16, what="prefill S8192 (sampled)")
     # query 0 sees one column (token 0): its output is that V row rounded to bf16
     v0 = d.w.win.kv[int(d.w.win.block_table[0, 0]), 0, 1]
     assert torch.equal(out[0].cpu(), v0.expand(d.w.num_heads, -1))
@@ -162,7 +164,7 @@ def test_edge_cases(case, mode):
     check_no_device_error()
     ref, _, _, err = run_oracle(w)
     assert not err
-    compare(out, ref, gate=MEAN_ABS_BF16_GATE, what=f"{case} {mode}")
+    compare(out, ref, gate=REL_MEAN_GATE_BF16, what=f"{case} {mode}")
     cols = d.columns().cpu().numpy().astype(np.int64)
     assert np.array_equal(cols, oracle_columns(w)[0])
 
@@ -187,7 +189,8 @@ def test_misaligned_pool_view_rejected():
     w = make("tiny_r4")
     d = OnDevice(w, dev)
     flat = d.win.kv.reshape(-1)
-    bad = flat[1:1 + flat.numel() - 64].reshape(d.win.kv.shape[0] - 1, *d.win.kv.shape[1:])
+    n = (d.win.kv.shape[0] - 1) * d.win.kv[0].numel()
+    bad = flat[1:1 + n].view(d.win.kv.shape[0] - 1, *d.win.kv.shape[1:])   # starts 2 bytes in
     pool = spa.PagedPool(bad, d.win.block_table)
     with pytest.raises(spa.SpaError) as e:
         spa.sparse_attn_paged_prefill(d.q, pool, d.cmp, d.tk, d.pos, **d.kw())
