@@ -121,6 +121,27 @@ int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * Decode that allocates nothing (the pages have no counterpart: this is a convenience of this
+ * library).  For callers that cannot call cudaMalloc where they decode - a host runtime whose
+ * device allocator belongs to someone else, or a decode step recorded into a CUDA graph that may
+ * not contain allocations.  Same computation and result as sparse_attn_paged_decode, with the
+ * caller still passing q, the pools and out; the split-K partials go to a scratch array built into
+ * the library (SPA_NOALLOC_SCRATCH_BYTES bytes on every device that loads it, held until the
+ * process exits) instead of a caller workspace.
+ *   - The first call on a device, with that device current, looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture on that device.
+ *   - Problems whose partials need more than SPA_NOALLOC_SCRATCH_BYTES (see
+ *     sparse_attn_paged_decode_workspace_size) are rejected with SPA_ERR_WORKSPACE.
+ *   - Every call on a device shares the one array and leaves its partials there: two calls that
+ *     can overlap on the GPU (different streams without ordering between them) race and give
+ *     wrong results.  Calls ordered on one stream are safe.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define SPA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int sparse_attn_paged_decode_noalloc(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                                     const spa_problem_t* prob, void* out, void* stream);
+
+/*
  * Column dump (the integer half of the method, exposed for exact checks): cols[T][W + K] gets
  * the physical row of every column, window columns as the row itself, top-k columns as
  * (1 << 30) | row, and -1 where the column does not exist.  Uses the same device resolution

@@ -20,7 +20,8 @@ import torch
 __all__ = [
     "PagedPool", "SpaError", "library_path", "load_library", "sparse_attn_paged_prefill",
     "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8",
-    "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_resolve_columns",
+    "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
+    "sparse_attn_paged_resolve_columns",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -83,6 +84,8 @@ def load_library():
         f = getattr(lib, name)
         f.argtypes = [P, PP, PP, PR, P, P, ctypes.c_size_t, P]
         f.restype = ctypes.c_int
+    lib.sparse_attn_paged_decode_noalloc.argtypes = [P, PP, PP, PR, P, P]
+    lib.sparse_attn_paged_decode_noalloc.restype = ctypes.c_int
     lib.sparse_attn_paged_decode_workspace_size.argtypes = [PR]
     lib.sparse_attn_paged_decode_workspace_size.restype = ctypes.c_size_t
     lib.sparse_attn_paged_resolve_columns.argtypes = [PP, PP, PR, P, P]
@@ -209,6 +212,25 @@ def sparse_attn_paged_decode(q, win, cmp, topk_idx, positions, **kw):
 
 def sparse_attn_paged_decode_fp8(q, win, cmp, topk_idx, positions, **kw):
     return _decode(True, q, win, cmp, topk_idx, positions, **kw)
+
+
+def sparse_attn_paged_decode_noalloc(q, win, cmp, topk_idx, positions, *, window, ratio, scale,
+                                     seq_of_token=None, out=None, num_seqs=None, stream=None):
+    """Decode whose split-K partials use the library's built-in scratch array instead of a
+    workspace (for callers that cannot allocate device memory where they decode).  `out` must be
+    passed by such a caller; without it this wrapper allocates one with torch for convenience."""
+    lib = load_library()
+    _check_q(q)
+    if out is None:
+        out = torch.empty_like(q)
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    w, c = _pool_c(win, False), _pool_c(cmp, False)
+    st = lib.sparse_attn_paged_decode_noalloc(q.data_ptr(), ctypes.byref(w),
+                                              ctypes.byref(c) if c is not None else None,
+                                              ctypes.byref(prob), out.data_ptr(), _stream(stream))
+    if st != 0:
+        raise SpaError(st, "sparse_attn_paged_decode_noalloc")
+    return out
 
 
 def sparse_attn_paged_resolve_columns(win, cmp, topk_idx, positions, *, window, ratio,

@@ -1,0 +1,83 @@
+"""The decode entry point that allocates nothing, against the ordinary decode entry point.
+
+Some callers cannot call cudaMalloc where they decode (their allocator belongs to another runtime,
+or the decode step is being recorded into a CUDA graph that may hold no allocation).  For them
+sparse_attn_paged_decode_noalloc keeps the split-K partials in a scratch array built into the
+library.  This file is collected last so that a run stopping at the first failure has already run
+every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_paged_attention_gb300 as spa
+from workloads import make
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+SCRATCH_BYTES = 16 << 20      # SPA_NOALLOC_SCRATCH_BYTES in include/sparse_attn_paged.h
+
+
+def _call_noalloc_c(lib, d, out):
+    """Straight through the C ABI: q, pools, problem and out; no workspace argument."""
+    w = d["w"]
+    prob = spa._problem_c(d["q"], d["win"], d["tk"], d["pos"], d["sot"], w.window, w.ratio,
+                          w.scale, None)
+    win = spa._pool_c(d["win"], False)
+    cmp = spa._pool_c(d["cmp"], False) if d["cmp"] is not None else None
+    return lib.sparse_attn_paged_decode_noalloc(
+        d["q"].data_ptr(), ctypes.byref(win), ctypes.byref(cmp) if cmp is not None else None,
+        ctypes.byref(prob), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def _on_device(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = make(name)
+    dev = torch.device("cuda:0")
+    g = lambda t: None if t is None else t.to(dev)
+    return {"w": w, "q": g(w.q), "pos": g(w.positions), "sot": g(w.seq_of_token),
+            "tk": g(w.topk_idx) if w.topk > 0 else None,
+            "win": spa.PagedPool(g(w.win.kv), g(w.win.block_table)),
+            "cmp": None if w.cmp is None else spa.PagedPool(g(w.cmp.kv), g(w.cmp.block_table))}
+
+
+@pytest.mark.parametrize("name", ["decode_b8_r4", "decode_b1_r4", "tiny_r4"])
+def test_noalloc_matches_decode_twice(name):
+    d = _on_device(name)
+    lib = spa.load_library()
+    w = d["w"]
+    ref = spa.sparse_attn_paged_decode(d["q"], d["win"], d["cmp"], d["tk"], d["pos"],
+                                       window=w.window, ratio=w.ratio, scale=w.scale,
+                                       seq_of_token=d["sot"])
+    ref_np = ref.float().cpu().numpy()
+    for _ in range(2):                      # the shared scratch keeps the previous call's partials
+        out = torch.full_like(d["q"], float("nan"))
+        assert _call_noalloc_c(lib, d, out) == 0
+        assert spa.sparse_attn_paged_check_errors() == 0
+        err = np.abs(out.float().cpu().numpy() - ref_np)
+        assert np.all(np.isfinite(err))
+        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    d = _on_device("decode_b8_r4")
+    lib = spa.load_library()
+    w = d["w"]
+    # 4096 tokens of 64 heads x 512 need far more partial storage than the built-in array holds
+    q = torch.zeros((4096, 64, 512), dtype=torch.bfloat16, device=d["q"].device)
+    pos = torch.full((4096,), 32767, dtype=torch.int32, device=q.device)
+    sot = torch.zeros(4096, dtype=torch.int32, device=q.device)
+    tk = torch.full((4096, 512), -1, dtype=torch.int32, device=q.device)
+    big = dict(d, q=q, pos=pos, sot=sot, tk=tk)
+    need = spa.sparse_attn_paged_decode_workspace_size(q, d["win"], tk, pos, window=w.window,
+                                                       ratio=w.ratio, scale=w.scale,
+                                                       seq_of_token=sot)
+    assert need > SCRATCH_BYTES
+    out = torch.empty_like(q)
+    assert _call_noalloc_c(lib, big, out) == spa.SPA_STATUS["SPA_ERR_WORKSPACE"]
+
