@@ -118,8 +118,13 @@ void decode_plan(const spa_problem_t* pr, int sms, int* splits, int* cols) {
   int c = (int)((C + want - 1) / want);
   c = ((c + 31) / 32) * 32;
   if (c > C) c = C;
+  int n = (C + c - 1) / c;
+  if (n > spa::merge_max_splits()) {  // the merge reads at most this many partials per head
+    c = (C + spa::merge_max_splits() - 1) / spa::merge_max_splits();
+    n = (C + c - 1) / c;
+  }
   *cols = c;
-  *splits = (C + c - 1) / c;
+  *splits = n;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -134,7 +139,6 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   int st = validate(q, win, cmp, pr, out, fp8);
   if (st) return st;
   if (pr->num_tokens == 0) return SPA_OK;
-  if (fp8) return SPA_ERR_UNSUPPORTED;  // e4m3 pools: not in this build yet
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
   if (st) return st;
@@ -173,7 +177,7 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   p.n_items = (int)items;
   const int grid = (int)(items < sms ? items : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = spa::launch_attn_bf16(p, grid, s);
+  cudaError_t e = spa::launch_attn(p, grid, fp8, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   if (decode) {
     e = spa::launch_merge(p, s);

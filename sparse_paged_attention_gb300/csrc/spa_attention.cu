@@ -8,17 +8,27 @@
 //                        per-column choice of window or compressed pool), then copy the 16-byte
 //                        pieces of every K and V row into shared memory with cp.async, already in
 //                        the 128-byte-swizzled operand layout, through a 4-slot ring.
-//   MMA warp (4)         S^T[c][h] = K[c][:] . Q[h][:]    tcgen05, M = 128 columns, N = 64 heads
+//   MMA warp (4)         S^T[c][h] = K[c][:] . Q[h][:]    tcgen05, M = 128 columns, N = heads
 //                        O^T[d][h] += V[c][d] * P^T[c][h] tcgen05, M = 128 of head_dim, N = 64
 //                        both accumulate in TMEM (S^T double-buffered, O^T resident).
 //   softmax warps (0..3) one thread per column: read S^T from TMEM, mask, online max and sum
-//                        across columns (warp shuffles plus a 4-warp exchange), write P^T (bf16)
-//                        to shared memory; at the end divide O by the denominators and store.
+//                        across columns (warp shuffles plus a 4-warp exchange), write P^T to
+//                        shared memory; at the end divide O by the denominators and store.
 //
 // Heads sit in the N dimension, columns (and head_dim) in M = 128: an M = 128 tcgen05 tile runs
 // the tensor core at its full per-SM rate and keeps one TMEM lane per row, which a 64-row tile of
 // heads would not.
+//
+// e4m3 pools (FreeToken clone PR 3, "Perf/kv fp8 read path", part 1): K and V codes reach the
+// MMA unwidened (kind::f8f6f4, both operands e4m3).  q is split into q_hi + q_lo, two e4m3 terms
+// (times a power of two per token) that the S MMA reads as N = 128 rows, so the sum of the two
+// accumulator halves carries q to about bf16 precision.  The per-row K scale multiplies the scores
+// in fp32.  The probabilities are scaled by the per-row V scale (and a power of two per item),
+// split the same way into two e4m3 terms, and both accumulate into the same O; the softmax
+// denominator sums the unscaled fp32 probabilities.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "spa_launch.h"
 
@@ -27,24 +37,28 @@ namespace spa {
 namespace cfg {
 constexpr int kThreads = kAttnThreads;
 constexpr int kStages = 4;            // K/V ring slots
-constexpr int kSlotBytes = 32768;     // 128 rows x 128 head_dim values (two swizzle atoms)
+constexpr int kSlotBytes = 32768;     // 128 rows x 256 bytes (two 128-byte swizzle atoms)
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
-constexpr int kQAtomBytes = 8192;     // 64 heads x 128 bytes
 constexpr int kTi = 4;                // tile-info ring entries
 constexpr int kTmemCols = 512;
-constexpr int kOCol = 128;            // O^T chunks start at TMEM column 128 (S^T uses 0..127)
-constexpr float kTau = 8.0f;          // lazy rescale: keep the running max until it grows by 2^8
+
+struct TileInfo {                     // one entry of the tile-info ring
+  int item, n, flags, pad;
+  float q_scale, p_scale, pad1, pad2; // e4m3 only: 2^k applied to q and to the probabilities
+  float k_scale[128];                 // e4m3 only: per-column K and V scales of this tile
+  float v_scale[128];
+};
 
 constexpr int kRingOff = 0;
-constexpr int kQOff = kRingOff + kStages * kSlotBytes;      // 131072
-constexpr int kPOff = kQOff + 8 * kQAtomBytes;              // 196608
-constexpr int kListOff = kPOff + 128 * 128;                 // 212992
+constexpr int kQOff = kRingOff + kStages * kSlotBytes;      // 131072 (64 KB)
+constexpr int kPOff = kQOff + 65536;                        // 196608 (16 KB)
+constexpr int kListOff = kPOff + 16384;                     // 212992
 constexpr int kRedOff = kListOff + kMaxColumns * 4;         // 217088  float [2][4][64]
 constexpr int kMrowOff = kRedOff + 2 * 4 * 64 * 4;          // 219136  float [4][64]
 constexpr int kArowOff = kMrowOff + 4 * 64 * 4;             // 220160  float [4][64]
-constexpr int kTiOff = kArowOff + 4 * 64 * 4;               // 221184  int4 [kTi]
-constexpr int kCntOff = kTiOff + kTi * 16;                  // 221248  int [8]
-constexpr int kBarOff = kCntOff + 32;                       // 221280
+constexpr int kTiOff = kArowOff + 4 * 64 * 4;               // 221184  TileInfo [kTi]
+constexpr int kCntOff = kTiOff + kTi * (int)sizeof(TileInfo);
+constexpr int kBarOff = kCntOff + 64;
 
 enum {
   B_FULL = 0, B_EMPTY = 4, B_QFULL = 8, B_QEMPTY = 9, B_SFULL = 10, B_SEMPTY = 12,
@@ -53,10 +67,20 @@ enum {
 };
 constexpr int kMiscOff = kBarOff + B_COUNT * 8;             // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;            // + slack to align the base to 1 KB
+static_assert(sizeof(TileInfo) % 16 == 0, "tile info alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr int kFirst = 1, kLast = 2;
 }  // namespace cfg
+
+template <bool kFp8>
+struct Mode {
+  static constexpr int kElt = kFp8 ? 1 : 2;        // bytes per K/V element
+  static constexpr int kSCols = kFp8 ? 128 : 64;   // N of the S MMA (q, or q_hi | q_lo)
+  static constexpr int kOCol = 2 * kSCols;         // first TMEM column of O^T
+  static constexpr int kQAtom = kSCols * 128;      // bytes of one 128-byte-wide Q atom
+  static constexpr float kTau = kFp8 ? 4.0f : 8.0f;  // lazy rescale threshold (log2 units)
+};
 
 int attn_smem_bytes() { return cfg::kSmemBytes; }
 
@@ -112,6 +136,12 @@ __device__ __forceinline__ float xreduce32(const float (&v)[32], int lane) {
   return kMax ? fmaxf(keep, o) : keep + o;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // A wait whose outcome is the same on every lane of the warp (the softmax warps shuffle right
 // after their waits, so a lane must never leave the loop alone).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -130,15 +160,52 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-__global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __grid_constant__ AttnParams p) {
+// 2^floor(log2 x) for finite x > 0 (clears the mantissa; x is kept within the normal range).
+__device__ __forceinline__ float pow2_floor(float x) {
+  x = fminf(fmaxf(x, 1.17549435e-38f), 1.0e38f);
+  return __int_as_float(__float_as_int(x) & 0x7F800000);
+}
+
+// Two fp32 values -> two e4m3 codes (round to nearest even, saturating), first value low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t v) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&r));
+}
+// (a, b) -> hi = e4m3(a, b), lo = e4m3(a - hi_a, b - hi_b): hi + lo carries about 8 bits.
+__device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = e4m3x2(a, b);
+  const float2 h = e4m3x2_value(hi);
+  lo = e4m3x2(a - h.x, b - h.y);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// tcgen05 shared-memory descriptor, 64-byte swizzle (used for the e4m3 P^T operand).
+__device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using namespace cfg;
+  using M = Mode<kFp8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMiscOff + 4);
-  int4* ti = reinterpret_cast<int4*>(sm + kTiOff);
+  TileInfo* ti = reinterpret_cast<TileInfo*>(sm + kTiOff);
 #define BAR(i) (sb + (uint32_t)kBarOff + 8u * (uint32_t)(i))
 
   if (threadIdx.x == 0) {
@@ -171,8 +238,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kMiscOff);
 
   const int D = p.D;
-  const int n_datoms = D >> 6;          // 64-wide head_dim blocks (128 bytes of bf16)
-  const int n_chunks = (D + 127) >> 7;  // 128-wide head_dim chunks (one ring slot each)
+  const int P16 = D * M::kElt / 16;       // 16-byte pieces per K (or V) row
+  const int n_atoms = (P16 + 7) >> 3;     // 128-byte swizzle atoms per row
+  const int n_chunks = (n_atoms + 1) >> 1;  // ring slots per K tile (and per V tile)
+  const int n_ks = P16 >> 1;              // 32-byte K steps of the S MMA
+  const int n_mt = (D + 127) >> 7;        // 128-wide head_dim tiles of O^T
   const int C = p.rs.W + p.rs.K;
 
   if (warp >= 5) {
@@ -181,8 +251,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
     const int pw = warp - 5;
     int32_t* list = reinterpret_cast<int32_t*>(sm + kListOff);
     volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);
+    volatile float* fred = reinterpret_cast<volatile float*>(sm + kCntOff + 32);
     const int jj = ptid & 7, r0 = ptid >> 3;
-    const size_t row_bytes = (size_t)4 * D;  // K row then V row, bf16
+    const size_t row_bytes = (size_t)2 * D * M::kElt;  // K row then V row
     int ring = 0, tik = 0;
     uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
@@ -202,9 +273,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
       const int pos = __ldg(p.rs.positions + t);
       // resolve and compact the column set of this item
       int n = 0;
+      float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
       for (int c0 = c_lo; c0 < c_hi; c0 += 128) {
         const int c = c0 + ptid;
         const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t, b, pos, c) : -1;
+        if (kFp8 && code >= 0) {
+          const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
+          vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));
+        }
         const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
         if (lane == 0) cnt[pw] = __popc(m);
         named_bar_sync(2, 128);
@@ -219,33 +295,114 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
         n += tot;
         named_bar_sync(2, 128);
       }
+      float q_scale = 1.f, p_scale = 1.f;
+      if (kFp8 && n > 0) {
+        vmax = warp_max(vmax);
+        if (lane == 0) fred[pw] = vmax;
+        named_bar_sync(2, 128);
+        vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+        named_bar_sync(2, 128);
+        // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
+        p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
+      }
       const int n_tiles = (n + 127) >> 7;
       const int n_ti = n_tiles > 0 ? n_tiles : 1;
-      for (int j = 0; j < n_ti; ++j) {
-        mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-        if (ptid == 0) {
-          const int nj = n == 0 ? 0 : min(128, n - j * 128);
-          const int flags = (j == 0 ? kFirst : 0) | (j == n_ti - 1 ? kLast : 0);
-          ti[tik] = make_int4(item, nj, flags, 0);
-          mbar_arrive(BAR(B_TIFULL + tik));
-        }
-        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-        if (n == 0) break;
-        if (j == 0) {
-          // Q of this token and head group -> [atom][head][128 B], heads beyond H zero-filled
-          mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
-          q_ph ^= 1;
-          const uint32_t qs = sb + kQOff;
-          for (int it = 0; it < 4 * n_datoms; ++it) {
+      if (n > 0) {
+        // Q of this token and head group
+        mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
+        q_ph ^= 1;
+        const uint32_t qs = sb + kQOff;
+        if (!kFp8) {
+          // bf16: [atom][64 heads][128 B], heads beyond H zero-filled
+          for (int it = 0; it < 4 * n_atoms; ++it) {
             const int h = (it & 3) * 16 + r0;
             const int a = it >> 2;
             const int hg = g * 64 + h;
             const bool ok = hg < p.H;
             const uint8_t* src = p.q + (((size_t)t * p.H + (ok ? hg : 0)) * D) * 2 + a * 128 + jj * 16;
-            cp_async_16(qs + a * kQAtomBytes + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
+            cp_async_16(qs + a * M::kQAtom + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
           }
           cp_async_arrive_noinc(BAR(B_QFULL));
+        } else {
+          // e4m3: rows 0..63 hold q_hi, rows 64..127 q_lo, both times a power of two per token
+          float qm = 0.f;
+          for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+              qm = warp_max(qm);
+              if (lane == 0) fred[pw] = qm;
+              named_bar_sync(2, 128);
+              qm = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+              named_bar_sync(2, 128);
+              q_scale = qm > 0.f ? pow2_floor(448.f / qm) : 1.f;
+            }
+            for (int it = 0; it < 4 * n_atoms; ++it) {
+              const int h = (it & 3) * 16 + r0;
+              const int a = it >> 2;
+              const int piece = a * 8 + jj;      // 16 head_dim values
+              const int hg = g * 64 + h;
+              const bool ok = hg < p.H && piece < P16;
+              uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
+              if (ok) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.q + (((size_t)t * p.H + hg) * D + piece * 16) * 2);
+                u0 = __ldg(src);
+                u1 = __ldg(src + 1);
+              }
+              const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+              if (pass == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+              } else {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  uint32_t h0, l0, h1, l1;
+                  split_e4m3x2(bf16_lo(w[2 * k]) * q_scale, bf16_hi(w[2 * k]) * q_scale, h0, l0);
+                  split_e4m3x2(bf16_lo(w[2 * k + 1]) * q_scale, bf16_hi(w[2 * k + 1]) * q_scale, h1, l1);
+                  hi[k] = h0 | (h1 << 16);
+                  lo[k] = l0 | (l1 << 16);
+                }
+                uint8_t* qrow = sm + kQOff + a * M::kQAtom;
+                *reinterpret_cast<uint4*>(qrow + h * 128 + ((jj ^ (h & 7)) << 4)) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(qrow + (64 + h) * 128 + ((jj ^ (h & 7)) << 4)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(BAR(B_QFULL));
         }
+      }
+      for (int j = 0; j < n_ti; ++j) {
+        // publish this tile to the MMA and softmax warps
+        mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+        if (kFp8) {
+          const int idx = j * 128 + ptid;
+          const int32_t code = idx < n ? list[idx] : -1;
+          float ks = 0.f, vs = 0.f;
+          if (code >= 0) {
+            const bool cmp = code >> kColPoolShift;
+            const int row = code & ((1 << kColPoolShift) - 1);
+            ks = __ldg((cmp ? p.rs.cmp.k_scale : p.rs.win.k_scale) + row);
+            vs = __ldg((cmp ? p.rs.cmp.v_scale : p.rs.win.v_scale) + row);
+          }
+          ti[tik].k_scale[ptid] = ks;
+          ti[tik].v_scale[ptid] = vs;
+          named_bar_sync(2, 128);
+        }
+        if (ptid == 0) {
+          TileInfo& e = ti[tik];
+          e.item = item;
+          e.n = n == 0 ? 0 : min(128, n - j * 128);
+          e.flags = (j == 0 ? kFirst : 0) | (j == n_ti - 1 ? kLast : 0);
+          e.q_scale = q_scale;
+          e.p_scale = p_scale;
+          mbar_arrive(BAR(B_TIFULL + tik));
+        }
+        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+        if (n == 0) break;
         // the 8 rows of this tile that this thread copies
         const uint8_t* src[8];
 #pragma unroll
@@ -268,9 +425,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
               const int r = k * 16 + r0;
 #pragma unroll
               for (int aa = 0; aa < 2; ++aa) {
-                const int atom = 2 * kc + aa;
-                if (atom < n_datoms) {
-                  const uint8_t* sp = src[k] ? src[k] + half * (2 * D) + atom * 128 + jj * 16 : p.q;
+                const int piece = (2 * kc + aa) * 8 + jj;
+                if (piece < P16) {
+                  const uint8_t* sp = src[k] ? src[k] + half * (D * M::kElt) + piece * 16 : p.q;
                   cp_async_16(slot + aa * kAtomBytes + r * 128 + ((jj ^ (r & 7)) << 4), sp,
                               src[k] ? 16u : 0u);
                 }
@@ -286,7 +443,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
     if (!*abort_flag) {
       mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
       if (ptid == 0) {
-        ti[tik] = make_int4(-1, 0, kFirst | kLast, 0);
+        ti[tik].item = -1;
+        ti[tik].n = 0;
+        ti[tik].flags = kFirst | kLast;
         mbar_arrive(BAR(B_TIFULL + tik));
       }
     }
@@ -294,29 +453,32 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
   } else if (warp == 4) {
     // ====================================== MMA ========================================
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16(128, 64, 0, 0);  // A = K rows (K-major), B = Q (K-major)
-      const uint32_t idO = idesc_bf16(128, 64, 1, 1);  // A = V^T (MN-major), B = P^T (MN-major)
+      // S: A = K rows (K-major), B = q rows (K-major).  O: A = V^T (MN-major), B = P^T (MN-major)
+      const uint32_t idS = kFp8 ? idesc_e4m3(128, 128, 0, 0) : idesc_bf16(128, 64, 0, 0);
+      const uint32_t idO = kFp8 ? idesc_e4m3(128, 64, 1, 1) : idesc_bf16(128, 64, 1, 1);
       const uint32_t qbase = sb + kQOff, pbase = sb + kPOff;
       int ring = 0, tik = 0, sbuf = 0;
       uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
       for (;;) {
         if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
-        const int4 e = ti[tik];
+        const int n = ti[tik].n;
+        const int item = ti[tik].item;
+        const int flags = ti[tik].flags;
         mbar_arrive(BAR(B_TIEMPTY + tik));
         if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-        if (e.x < 0) break;
-        const int n = e.y;
+        if (item < 0) break;
         if (n == 0) continue;
-        const bool first = e.z & kFirst, last = e.z & kLast;
+        const bool first = flags & kFirst, last = flags & kLast;
         if (first) {
           if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;
           q_ph ^= 1;
         }
         if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) break;
         s_ph ^= 1u << sbuf;
+        fence_proxy_async_smem();
         tc_fence_after();
         bool ok = true;
-        const uint32_t dS = tmem + sbuf * 64;
+        const uint32_t dS = tmem + sbuf * M::kSCols;
         for (int kc = 0; kc < n_chunks; ++kc) {
           if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
           fence_proxy_async_smem();
@@ -324,12 +486,16 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
           const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
           for (int aa = 0; aa < 2; ++aa) {
             const int atom = 2 * kc + aa;
-            if (atom >= n_datoms) break;
+            if (atom >= n_atoms) break;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
+              if (atom * 4 + ks >= n_ks) break;
               const uint64_t da = sdesc(slot + aa * kAtomBytes + ks * 32, 16, 1024);
-              const uint64_t db = sdesc(qbase + atom * kQAtomBytes + ks * 32, 16, 1024);
-              mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
+              const uint64_t db = sdesc(qbase + atom * M::kQAtom + ks * 32, 16, 1024);
+              if (kFp8)
+                mma_f8(dS, da, db, idS, (kc | aa | ks) != 0);
+              else
+                mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
             }
           }
           mma_commit(BAR(B_EMPTY + ring));
@@ -347,17 +513,36 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
         }
         fence_proxy_async_smem();
         tc_fence_after();
-        const int nk = (n + 15) >> 4;
         for (int vc = 0; vc < n_chunks; ++vc) {
           if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
-          const uint32_t dO = tmem + kOCol + vc * 64;
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t da = sdesc(slot + kk * 2048, kAtomBytes, 1024);
-            const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
-            mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
+          if (!kFp8) {
+            // one 128-wide head_dim tile per slot (two 64-wide atoms, LBO apart); K = 16 columns
+            const uint32_t dO = tmem + M::kOCol + vc * 64;
+            const int nk = (n + 15) >> 4;
+            for (int kk = 0; kk < nk; ++kk) {
+              const uint64_t da = sdesc(slot + kk * 2048, kAtomBytes, 1024);
+              const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+              mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
+            }
+          } else {
+            // two 128-wide head_dim tiles per slot (one atom each); K = 32 columns; P^T is
+            // p_hi (64-byte rows, 64-byte swizzle) followed by p_lo, both into the same O
+            const int nk = (n + 31) >> 5;
+            for (int aa = 0; aa < 2; ++aa) {
+              const int mt = 2 * vc + aa;
+              if (mt >= n_mt) break;
+              const uint32_t dO = tmem + M::kOCol + mt * 64;
+              for (int kk = 0; kk < nk; ++kk) {
+                const uint64_t da = sdesc(slot + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
+                const uint64_t dh = sdesc64(pbase + kk * 2048, 8192, 512);
+                const uint64_t dl = sdesc64(pbase + 8192 + kk * 2048, 8192, 512);
+                mma_f8(dO, da, dh, idO, (first && kk == 0) ? 0u : 1u);
+                mma_f8(dO, da, dl, idO, 1u);
+              }
+            }
           }
           mma_commit(BAR(B_EMPTY + ring));
           if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
@@ -380,22 +565,30 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
     const float sl2 = p.scale_log2;
     int tik = 0, sbuf = 0, rb = 0;
     uint32_t ti_ph = 0, s_ph = 0, pv_ph = 0, red_ph = 0;
-    // running max (base-2 units) and this warp's partial denominator of heads 2*lane, 2*lane+1
+    // running max (base-2 units) and this warp's partial denominator of heads lane, 32 + lane
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float p_scale = 1.f;
     int t = 0, g = 0, s = 0;
     bool had = false;
     for (;;) {
       if (!warp_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
-      const int4 e = ti[tik];
+      const int item = ti[tik].item;
+      const int n = ti[tik].n;
+      const int flags = ti[tik].flags;
+      float col_scale = sl2, v_fold = 0.f;
+      if (kFp8) {
+        col_scale = sl2 * ti[tik].k_scale[tid] / ti[tik].q_scale;
+        p_scale = ti[tik].p_scale;
+        v_fold = ti[tik].v_scale[tid] * p_scale;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_TIEMPTY + tik));
       if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-      if (e.x < 0) break;
-      const int n = e.y;
-      const bool first = e.z & kFirst, last = e.z & kLast;
+      if (item < 0) break;
+      const bool first = flags & kFirst, last = flags & kLast;
       if (first) {
-        s = e.x % p.n_splits;
-        const int tg = e.x / p.n_splits;
+        s = item % p.n_splits;
+        const int tg = item / p.n_splits;
         g = tg % p.n_groups;
         t = tg / p.n_groups;
         m0 = m1 = -INFINITY;
@@ -408,16 +601,24 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
         s_ph ^= 1u << sbuf;
         tc_fence_after();
         const bool valid = tid < n;
-        const uint32_t s_addr = lane_base + sbuf * 64;
+        const uint32_t s_addr = lane_base + sbuf * M::kSCols;
         float* rr = red + rb * 256;
         // pass 1: tile maximum of every head (lane L ends up with heads L and 32 + L)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
           tmem_ld32(s_addr + hf * 32, x);
-          tmem_wait_ld();
+          if (kFp8) {
+            float y[32];
+            tmem_ld32(s_addr + 64 + hf * 32, y);
+            tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = valid ? x[k] * sl2 : -INFINITY;
+            for (int k = 0; k < 32; ++k) x[k] += y[k];
+          } else {
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = valid ? x[k] * col_scale : -INFINITY;
           rr[warp * 64 + hf * 32 + lane] = xreduce32<true>(x, lane);
         }
         __syncwarp();
@@ -431,8 +632,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
           M1 = fmaxf(M1, rr[w * 64 + 32 + lane]);
         }
         rb ^= 1;
-        const float n0 = (M0 > m0 + kTau) ? M0 : m0;
-        const float n1 = (M1 > m1 + kTau) ? M1 : m1;
+        const float n0 = (M0 > m0 + M::kTau) ? M0 : m0;
+        const float n1 = (M1 > m1 + M::kTau) ? M1 : m1;
         const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
         const bool grow = __any_sync(0xffffffffu, (n0 != m0) || (n1 != m1));
         m0 = n0;
@@ -444,11 +645,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
         __syncwarp();
         if (grow && !first) {
           // the running max moved: rescale O (its last PV finished before this S was ready)
-          for (int i = 0; i < n_chunks; ++i) {
+          for (int i = 0; i < n_mt; ++i) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               float o[32];
-              const uint32_t ta = lane_base + kOCol + i * 64 + hf * 32;
+              const uint32_t ta = lane_base + M::kOCol + i * 64 + hf * 32;
               tmem_ld32(ta, o);
               tmem_wait_ld();
 #pragma unroll
@@ -465,29 +666,59 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
           if (!warp_wait(BAR(B_PVDONE), pv_ph, abort_flag)) break;
           pv_ph ^= 1;
         }
-        // pass 2: probabilities, P^T row of this column (bf16), this warp's denominators
-        uint8_t* prow = sm + kPOff + tid * 128;
+        // pass 2: probabilities, P^T row of this column, this warp's denominators
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
           tmem_ld32(s_addr + hf * 32, x);
-          tmem_wait_ld();
+          if (kFp8) {
+            float y[32];
+            tmem_ld32(s_addr + 64 + hf * 32, y);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] += y[k];
+          } else {
+            tmem_wait_ld();
+          }
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            x[k] = valid ? fast_exp2(x[k] * sl2 - mrow[hf * 32 + k]) : 0.f;
+            x[k] = valid ? fast_exp2(x[k] * col_scale - mrow[hf * 32 + k]) : 0.f;
+          if (!kFp8) {
+            uint8_t* prow = sm + kPOff + tid * 128;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int k = hf * 4 + q4;  // 16-byte chunk: heads 8k .. 8k+7
-            uint4 u;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(x[8 * q4 + 0], x[8 * q4 + 1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(x[8 * q4 + 2], x[8 * q4 + 3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q4 + 4], x[8 * q4 + 5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(x[8 * q4 + 6], x[8 * q4 + 7]);
-            u.x = *reinterpret_cast<uint32_t*>(&b0);
-            u.y = *reinterpret_cast<uint32_t*>(&b1);
-            u.z = *reinterpret_cast<uint32_t*>(&b2);
-            u.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(prow + ((k ^ (tid & 7)) << 4)) = u;
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int k = hf * 4 + q4;  // 16-byte chunk: heads 8k .. 8k+7
+              uint4 u;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(x[8 * q4 + 0], x[8 * q4 + 1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(x[8 * q4 + 2], x[8 * q4 + 3]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q4 + 4], x[8 * q4 + 5]);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(x[8 * q4 + 6], x[8 * q4 + 7]);
+              u.x = *reinterpret_cast<uint32_t*>(&b0);
+              u.y = *reinterpret_cast<uint32_t*>(&b1);
+              u.z = *reinterpret_cast<uint32_t*>(&b2);
+              u.w = *reinterpret_cast<uint32_t*>(&b3);
+              *reinterpret_cast<uint4*>(prow + ((k ^ (tid & 7)) << 4)) = u;
+            }
+          } else {
+            // P * v_scale * p_scale as p_hi + p_lo (e4m3), 64-byte rows, 64-byte swizzle
+            uint8_t* ph = sm + kPOff + tid * 64;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int k = hf * 2 + q2;  // 16-byte chunk: heads 16k .. 16k+15
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                uint32_t h0, l0v, h1, l1v;
+                const float* xv = x + 16 * q2 + 4 * w;
+                split_e4m3x2(xv[0] * v_fold, xv[1] * v_fold, h0, l0v);
+                split_e4m3x2(xv[2] * v_fold, xv[3] * v_fold, h1, l1v);
+                hi[w] = h0 | (h1 << 16);
+                lo[w] = l0v | (l1v << 16);
+              }
+              const int off = (k ^ ((tid >> 1) & 3)) << 4;
+              *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(ph + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
           }
           const float ts = xreduce32<false>(x, lane);
           if (hf == 0) l0 += ts; else l1 += ts;
@@ -531,8 +762,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
           L1 += rr[w * 64 + 32 + lane];
         }
         rb ^= 1;
-        arow[lane] = 1.f / L0;
-        arow[32 + lane] = 1.f / L1;
+        arow[lane] = 1.f / (L0 * p_scale);
+        arow[32 + lane] = 1.f / (L1 * p_scale);
         __syncwarp();
         if (p.decode && warp == 0) {
           const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * 64;
@@ -547,10 +778,10 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
           const size_t row0 = (size_t)t * p.H + g * 64 + hf * 32;  // first head of this half
           const int nh = min(32, Hg - hf * 32);                     // heads of this half present
 #pragma unroll 1
-          for (int i = 0; i < n_chunks; ++i) {
+          for (int i = 0; i < n_mt; ++i) {
             const int d = i * 128 + tid;
             float o[32];
-            tmem_ld32(lane_base + kOCol + i * 64 + hf * 32, o);
+            tmem_ld32(lane_base + M::kOCol + i * 64 + hf * 32, o);
             tmem_wait_ld();
             if (d < D) {
               if (p.decode) {
@@ -590,32 +821,51 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_bf16_kernel(const __gri
 }
 
 // Log-sum-exp merge of the split partials (base-2 LSE): out = sum_s 2^(lse_s - L) O_s / sum_s
-// 2^(lse_s - L), L = max_s lse_s.  One block per (token, head).
+// 2^(lse_s - L), L = max_s lse_s.  One block per (token, head); all partial loads of a thread are
+// issued before any is used.
+constexpr int kMergeMaxSplits = 32;
+
 __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ ws_o,
                                                     const float* __restrict__ ws_lse,
                                                     __nv_bfloat16* __restrict__ out, int S, int H,
                                                     int D) {
+  __shared__ float w_s[kMergeMaxSplits];
+  __shared__ float inv_sum;
   const int t = blockIdx.x / H, h = blockIdx.x % H;
   const float* lse = ws_lse + (size_t)t * S * H + h;
-  float L = -INFINITY;
-  for (int s = 0; s < S; ++s) L = fmaxf(L, lse[(size_t)s * H]);
+  if (threadIdx.x < 32) {
+    const float l = threadIdx.x < S ? lse[(size_t)threadIdx.x * H] : -INFINITY;
+    const float L = warp_max(l);
+    const float w = (l == -INFINITY) ? 0.f : exp2f(l - L);
+    float sum = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (threadIdx.x < S) w_s[threadIdx.x] = w;
+    if (threadIdx.x == 0) inv_sum = sum > 0.f ? 1.f / sum : 0.f;
+  }
+  __syncthreads();
+  const float inv = inv_sum;
   for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (L > -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float l = lse[(size_t)s * H];
-        if (l == -INFINITY) continue;
-        const float w = exp2f(l - L);
-        const float4 o = *reinterpret_cast<const float4*>(ws_o + (((size_t)t * S + s) * H + h) * D + d);
-        wsum += w;
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+    for (int s0 = 0; s0 < S; s0 += 8) {     // eight partial loads in flight at a time
+      float4 o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (s0 + k < S)
+          o[k] = __ldg(reinterpret_cast<const float4*>(ws_o + (((size_t)t * S + s0 + k) * H + h) * D + d));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (s0 + k < S) {
+          const float w = w_s[s0 + k];
+          if (w != 0.f) {
+            acc.x += w * o[k].x;
+            acc.y += w * o[k].y;
+            acc.z += w * o[k].z;
+            acc.w += w * o[k].w;
+          }
+        }
       }
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     uint2 u;
@@ -636,14 +886,22 @@ __global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ c
 }
 
 cudaError_t prepare_attn_kernels() {
-  return cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               cfg::kSmemBytes);
 }
 
-cudaError_t launch_attn_bf16(const AttnParams& p, int grid, cudaStream_t stream) {
-  attn_bf16_kernel<<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
+cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t stream) {
+  if (fp8)
+    attn_kernel<true><<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
+  else
+    attn_kernel<false><<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
+
+int merge_max_splits() { return kMergeMaxSplits; }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream) {
   merge_kernel<<<p.rs.T * p.H, 128, 0, stream>>>(p.ws_o, p.ws_lse,

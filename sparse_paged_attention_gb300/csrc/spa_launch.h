@@ -27,7 +27,8 @@ constexpr int kAttnThreads = 288;     // 4 softmax warps + 1 MMA warp + 4 gather
 int attn_smem_bytes();
 constexpr int kMaxColumns = 1024;     // window + top-k columns per query
 
-cudaError_t launch_attn_bf16(const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t stream);
+int merge_max_splits();
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_resolve_dump(const ResolveArgs& a, int32_t* cols, cudaStream_t stream);
 cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)

@@ -207,3 +207,43 @@ def test_stream_and_repeatability():
     assert torch.equal(a, b)          # same inputs, same plan: bitwise identical
     c = d.prefill()
     assert torch.equal(d.prefill(), c)
+
+
+# --- e4m3 pools (FreeToken clone PR 3, "Perf/kv fp8 read path") -------------------------------
+
+REL_MEAN_GATE_FP8 = 2e-2
+
+
+def test_fp8_prefill_chunk_sampled():
+    d = OnDevice(make("prefill_fp8_s4096_r4"), _dev())
+    out = d.prefill()
+    check_no_device_error()
+    toks = _sample_tokens(d.w.num_tokens, 40, 2)
+    ref, _, _, _ = run_oracle(d.w, tokens=toks)
+    compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_FP8, what="fp8 prefill chunk (sampled)")
+
+
+FP8_EDGE = {
+    "fp8_decode_b1": dict(seqs=[[32767]], num_heads=64, window=128, topk=512, ratio=4,
+                          head_dim=512, page_size=64),
+    "fp8_d64_h8": dict(num_heads=8, window=16, topk=40, ratio=4, head_dim=64),
+    "fp8_d192_h20": dict(num_heads=20, window=50, topk=77, ratio=4, head_dim=192),
+    "fp8_h128_anywhere": dict(num_heads=128, window=33, topk=150, ratio=2, head_dim=256,
+                              topk_fill="anywhere"),
+    "fp8_ratio0": dict(num_heads=64, window=128, topk=0, ratio=0, head_dim=512),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FP8_EDGE))
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_fp8_cases(case, mode):
+    kw = dict(FP8_EDGE[case])
+    kw.setdefault("page_size", 16)
+    seqs = [np.array(s) for s in kw.pop("seqs", [[0, 5, 77, 300, 1500], [2, 999], [4095]])]
+    w = build(case, seq_positions=seqs, seed=11, fp8=True, decode=(mode == "decode"), **kw)
+    d = OnDevice(w, _dev())
+    out = d.prefill() if mode == "prefill" else d.decode()
+    check_no_device_error()
+    ref, _, _, err = run_oracle(w)
+    assert not err
+    compare(out, ref, gate=REL_MEAN_GATE_FP8, what=f"{case} {mode}")
