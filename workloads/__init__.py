@@ -271,7 +271,8 @@ def pool_rows_referenced(w: Workload) -> int:
     return total
 
 
-# Workloads named after what they are.  Sizes follow the FreeToken PR 633 "Kernel time" shapes.
+# Workloads named after what they are.  Sizes follow the FreeToken PR 633 "Kernel time" shapes
+# (64 heads, head_dim 512, window 128, top-k 512, page size 64).
 CONFIG_NAMES = (
     "tiny_r4",              # 16 queries @ 240..255, 8 heads, D 64, window 16, top-k 32 of 64 (r 4)
     "decode_b1_r4",         # B 1 @ 32767, 64 heads, D 512, window 128, top-k 512 of 8192 (r 4)
@@ -281,26 +282,32 @@ CONFIG_NAMES = (
     "prefill_s8192_r4",     # 8192 queries from position 0, top-k 512 (r 4)
     "prefill_fp8_s4096_r4", # e4m3 pools, 4096 queries at 28672..32767, top-k 512 of 8192 (r 4)
 )
+# The remaining shapes of the same table.
+PAGE_SHAPES = (
+    "prefill_s2048_r4", "prefill_s4096at28672_r4", "prefill_s8192_r128", "prefill_s8192_r0",
+    "decode_b1_r128", "decode_b1_r0",
+)
 
 
 def make(name: str, seed: int = 0) -> Workload:
     """The named workloads (seed 0 unless told otherwise)."""
+    big = dict(num_heads=64, head_dim=512, window=128, page_size=64, seed=seed)
+    topk_of = {128: 256, 4: 512, 0: 0}
     if name == "tiny_r4":
         return build(name, seq_positions=[np.arange(240, 256)], num_heads=8, head_dim=64,
                      window=16, topk=32, ratio=4, page_size=16, seed=seed, oversize=1)
-    if name == "decode_b1_r4":
-        return build(name, seq_positions=[np.array([32767])], num_heads=64, head_dim=512,
-                     window=128, topk=512, ratio=4, page_size=64, seed=seed, decode=True)
-    if name.startswith("decode_b8_r"):
-        r = int(name.rsplit("_r", 1)[1])
-        k = {128: 256, 4: 512, 0: 0}[r]
-        return build(name, seq_positions=[np.array([32767])] * 8, num_heads=64, head_dim=512,
-                     window=128, topk=k, ratio=r, page_size=64, seed=seed, decode=True)
-    if name == "prefill_s8192_r4":
-        return build(name, seq_positions=[np.arange(0, 8192)], num_heads=64, head_dim=512,
-                     window=128, topk=512, ratio=4, page_size=64, seed=seed)
+    if name.startswith("decode_b"):
+        bsz, r = name[len("decode_b"):].split("_r")
+        r = int(r)
+        return build(name, seq_positions=[np.array([32767])] * int(bsz), topk=topk_of[r],
+                     ratio=r, decode=True, **big)
     if name == "prefill_fp8_s4096_r4":
-        return build(name, seq_positions=[np.arange(28672, 32768)], num_heads=64, head_dim=512,
-                     window=128, topk=512, ratio=4, page_size=64, seed=seed, fp8=True,
-                     cmp_entries=[8192])
+        return build(name, seq_positions=[np.arange(28672, 32768)], topk=512, ratio=4, fp8=True,
+                     cmp_entries=[8192], **big)
+    if name == "prefill_s4096at28672_r4":
+        return build(name, seq_positions=[np.arange(28672, 32768)], topk=512, ratio=4, **big)
+    if name.startswith("prefill_s"):
+        S, r = name[len("prefill_s"):].split("_r")
+        r = int(r)
+        return build(name, seq_positions=[np.arange(0, int(S))], topk=topk_of[r], ratio=r, **big)
     raise KeyError(name)
