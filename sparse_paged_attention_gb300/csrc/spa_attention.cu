@@ -152,8 +152,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // A wait that must end even when the CTA is aborting (drain before releasing TMEM).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
+  for (uint32_t it = 1; !mbar_try_wait(bar, parity); ++it) {
+    if (it >= kWaitLimitPolls && globaltimer() - t0 > kWaitLimitNs) {
       flag_error(SPA_ERR_TIMEOUT);
       return;
     }

@@ -105,9 +105,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Time limit of one pipeline wait.  A wait that runs out raises SPA_ERR_TIMEOUT and sets the
-// CTA's abort flag, after which every role leaves its loop and the kernel ends cleanly.
+// Limits of one pipeline wait.  A wait gives up only after at least kWaitLimitPolls polls AND
+// kWaitLimitNs of wall-clock time: the poll count keeps a pause of the whole GPU (a debugger or
+// profiler stopping the kernel) from being mistaken for a stuck pipeline, the clock keeps fast
+// polls from giving up early.  Giving up raises SPA_ERR_TIMEOUT and sets the CTA's abort flag,
+// after which every role leaves its loop and the kernel ends cleanly.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitPolls = 1u << 20;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -116,7 +120,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (it >= kWaitLimitPolls && globaltimer() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
         flag_error(SPA_ERR_TIMEOUT);
         return false;
