@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
     volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);
     volatile float* fred = reinterpret_cast<volatile float*>(sm + kCntOff + 32);
     const int jj = ptid & 7, r0 = ptid >> 3;
+    // this thread copies chunk jj of rows r0, r0 + 16, ...: (r & 7) == (r0 & 7) for all of them
+    const uint32_t dst_thread = (uint32_t)(r0 * 128 + ((jj ^ (r0 & 7)) << 4));
     const size_t row_bytes = (size_t)2 * D * M::kElt;  // K row then V row
     int ring = 0, tik = 0;
     uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
@@ -416,21 +418,27 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
             src[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
           }
         }
+        // Rows the MMAs read: the S MMA masks columns >= nj in the softmax, so K rows past nj
+        // may hold anything; the PV MMA reads V rows up to its K-step multiple, which must be
+        // zero past nj (zero probability times a stale NaN would still be NaN).  Row groups of
+        // 16 past that bound are skipped with a warp-uniform test.
+        const int nj = min(128, n - j * 128);
+        const int pv_step = kFp8 ? 32 : 16;
+        const int v_rows = (nj + pv_step - 1) / pv_step * pv_step;
         for (int half = 0; half < 2; ++half) {      // K rows, then V rows
+          const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
           for (int kc = 0; kc < n_chunks; ++kc) {
             mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
-            const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+            const uint32_t d0 = sb + kRingOff + ring * kSlotBytes + dst_thread;
+            const bool a0 = (2 * kc) * 8 + jj < P16, a1 = (2 * kc + 1) * 8 + jj < P16;
+            const size_t so = (size_t)half * D * M::kElt + (size_t)(2 * kc) * 128 + jj * 16;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const int r = k * 16 + r0;
-#pragma unroll
-              for (int aa = 0; aa < 2; ++aa) {
-                const int piece = (2 * kc + aa) * 8 + jj;
-                if (piece < P16) {
-                  const uint8_t* sp = src[k] ? src[k] + half * (D * M::kElt) + piece * 16 : p.q;
-                  cp_async_16(slot + aa * kAtomBytes + r * 128 + ((jj ^ (r & 7)) << 4), sp,
-                              src[k] ? 16u : 0u);
-                }
+              if (k < kmax) {
+                const uint8_t* sp = src[k] ? src[k] + so : p.q;
+                const uint32_t sz = src[k] ? 16u : 0u;
+                if (a0) cp_async_16(d0 + k * 2048, sp, sz);
+                if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
               }
             }
             cp_async_arrive_noinc(BAR(B_FULL + ring));

@@ -111,7 +111,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // polls from giving up early.  Giving up raises SPA_ERR_TIMEOUT and sets the CTA's abort flag,
 // after which every role leaves its loop and the kernel ends cleanly.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kWaitLimitPolls = 1u << 20;
+constexpr uint32_t kWaitLimitPolls = 1u << 24;
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
