@@ -107,10 +107,14 @@ int sparse_attn_paged_prefill_fp8(const void* q, const spa_pool_t* win, const sp
 
 /*
  * Decode: split-K over the column set (FreeToken PR 633, call paths: the split-K decode kernel),
- * then a log-sum-exp merge of the per-split partials into out.  The caller passes a device
- * workspace of at least sparse_attn_paged_decode_workspace_size(prob) bytes (16-byte aligned);
- * its contents need no initialisation and are scratch after the call.  Two calls that run
- * concurrently must use different workspaces.
+ * then a log-sum-exp merge of the per-split partials into out.  When the queries leave SMs idle,
+ * the column set of each query is split over up to 16 CTAs that form one thread-block cluster and
+ * merge their partials through distributed shared memory, in the same kernel; when the queries
+ * alone fill the GPU there is no split.  Both plans need no workspace and
+ * sparse_attn_paged_decode_workspace_size returns 0 (workspace may then be NULL).  Only where
+ * clusters cannot be launched do the partials go through a device workspace of at least
+ * sparse_attn_paged_decode_workspace_size(prob) bytes (16-byte aligned, contents scratch; two
+ * concurrent calls need different workspaces) and a second, merge kernel.
  */
 size_t sparse_attn_paged_decode_workspace_size(const spa_problem_t* prob);
 int sparse_attn_paged_decode(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
@@ -125,13 +129,15 @@ int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa
  * library).  For callers that cannot call cudaMalloc where they decode - a host runtime whose
  * device allocator belongs to someone else, or a decode step recorded into a CUDA graph that may
  * not contain allocations.  Same computation and result as sparse_attn_paged_decode, with the
- * caller still passing q, the pools and out; the split-K partials go to a scratch array built into
- * the library (SPA_NOALLOC_SCRATCH_BYTES bytes on every device that loads it, held until the
- * process exits) instead of a caller workspace.
+ * caller still passing q, the pools and out.  This entry point always takes the split-K path with
+ * global partials and the merge kernel, and its partials go to a scratch array built into the
+ * library (SPA_NOALLOC_SCRATCH_BYTES bytes on every device that loads it, held until the process
+ * exits) instead of a caller workspace.
  *   - The first call on a device, with that device current, looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture on that device.
- *   - Problems whose partials need more than SPA_NOALLOC_SCRATCH_BYTES (see
- *     sparse_attn_paged_decode_workspace_size) are rejected with SPA_ERR_WORKSPACE.
+ *   - Problems whose partials need more than SPA_NOALLOC_SCRATCH_BYTES (fp32 [T][S][H][D]
+ *     partials plus [T][S][H] log-sum-exps, S splits per query) are rejected with
+ *     SPA_ERR_WORKSPACE.
  *   - Every call on a device shares the one array and leaves its partials there: two calls that
  *     can overlap on the GPU (different streams without ordering between them) race and give
  *     wrong results.  Calls ordered on one stream are safe.

@@ -23,6 +23,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sms[kMaxDevices];
 bool g_prepared[kMaxDevices];
+// clusters of 2, 4, 8, 16 attention CTAs that can be resident at once (both kernel variants)
+int g_clusters[kMaxDevices][5];
 
 // SM count of the current device; sets the kernels' shared-memory attribute once per device.
 int current_device(int* dev, int* sms) {
@@ -37,10 +39,23 @@ int current_device(int* dev, int* sms) {
     e = spa::prepare_attn_kernels();
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     g_sms[*dev] = n;
+    for (int i = 1; i <= 4; ++i) {
+      const int a = spa::attn_max_active_clusters(1 << i, false);
+      const int b = spa::attn_max_active_clusters(1 << i, true);
+      g_clusters[*dev][i] = a < b ? a : b;
+    }
     g_prepared[*dev] = true;
   }
   *sms = g_sms[*dev];
   return SPA_OK;
+}
+
+int max_active_clusters(int dev, int size) {
+  int i = 0;
+  while ((1 << i) < size) ++i;
+  if (i < 1 || i > 4) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_clusters[dev][i];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -108,8 +123,43 @@ void fill_resolve(spa::ResolveArgs& a, const spa_pool_t* win, const spa_pool_t* 
   a.r = uses_cmp(pr) ? pr->ratio : 0;
 }
 
-// Decode split plan: enough splits to give every SM one item, at least 32 columns per split.
-void decode_plan(const spa_problem_t* pr, int sms, int* splits, int* cols) {
+// Decode plan.  With T*G (token, head group) pairs and C columns per query:
+//  * T*G >= SMs/2: no split; each CTA attends over whole queries and writes the output directly.
+//  * otherwise the columns are split S ways (S a power of two <= 16, at least 16 columns per
+//    split, S*T*G CTAs at most one per SM) and the S CTAs of a pair form a thread-block cluster
+//    that merges the partial results through distributed shared memory: no workspace, no
+//    second kernel.  S shrinks until all T*G clusters fit on the device at once.
+//  * if no cluster size fits, the split-K partials go through the workspace and the merge
+//    kernel (decode_plan_ws).
+struct DecodePlan {
+  int splits, cols, cluster;  // cluster == 0 with splits > 1: workspace + merge kernel
+};
+
+void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols);
+
+DecodePlan decode_plan(const spa_problem_t* pr, int dev, int sms) {
+  const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
+  const long long groups = (pr->num_heads + 63) / 64;
+  const long long base = (long long)pr->num_tokens * groups;
+  DecodePlan pl{1, C, 0};
+  if (base <= 0 || 2 * base >= sms) return pl;
+  int S = 16;
+  while (S > 1 && ((long long)S * base > sms || (C + S - 1) / S < 16)) S >>= 1;
+  while (S > 1 && max_active_clusters(dev, S) < base) S >>= 1;
+  if (S > 1) {
+    pl.splits = S;
+    pl.cols = (C + S - 1) / S;
+    pl.cluster = S;
+    return pl;
+  }
+  if (max_active_clusters(dev, 2) >= 1) return pl;  // clusters work; one split is the best fit
+  decode_plan_ws(pr, sms, &pl.splits, &pl.cols);
+  return pl;
+}
+
+// Split plan of the workspace path: enough splits to give every SM one item, at least 32
+// columns per split.
+void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols) {
   const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
   const long long groups = (pr->num_heads + 63) / 64;
   const long long base = (long long)pr->num_tokens * groups;
@@ -135,7 +185,8 @@ size_t workspace_bytes(const spa_problem_t* pr, int splits) {
 }
 
 int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_problem_t* pr,
-        void* out, void* ws, size_t ws_bytes, void* stream, bool decode, bool fp8) {
+        void* out, void* ws, size_t ws_bytes, void* stream, bool decode, bool fp8,
+        bool force_partials = false) {
   int st = validate(q, win, cmp, pr, out, fp8);
   if (st) return st;
   if (pr->num_tokens == 0) return SPA_OK;
@@ -153,20 +204,28 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   p.n_groups = (pr->num_heads + 63) / 64;
   p.scale_log2 = pr->scale * 1.4426950408889634f;
   const int C = pr->window + pr->topk;
+  bool merge = false;
   if (decode) {
-    int splits = 1, cols = 1;
-    decode_plan(pr, sms, &splits, &cols);
-    const size_t need = workspace_bytes(pr, splits);
-    if (!ws) return SPA_ERR_NULL;
-    if (!aligned16(ws)) return SPA_ERR_ALIGN;
-    if (ws_bytes < need) return SPA_ERR_WORKSPACE;
-    const size_t tsh = (size_t)pr->num_tokens * splits * pr->num_heads;
-    p.ws_o = static_cast<float*>(ws);
-    p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                        align256(tsh * pr->head_dim * sizeof(float)));
-    p.n_splits = splits;
-    p.cols_per_split = cols;
-    p.decode = 1;
+    DecodePlan pl = decode_plan(pr, dev, sms);
+    if (force_partials && (pl.cluster > 1 || pl.splits == 1)) {
+      pl.cluster = 0;
+      decode_plan_ws(pr, sms, &pl.splits, &pl.cols);
+    }
+    p.n_splits = pl.splits;
+    p.cols_per_split = pl.cols;
+    p.cluster = pl.cluster;
+    if (pl.cluster == 0 && (pl.splits > 1 || force_partials)) {
+      const size_t need = workspace_bytes(pr, pl.splits);
+      if (!ws) return SPA_ERR_NULL;
+      if (!aligned16(ws)) return SPA_ERR_ALIGN;
+      if (ws_bytes < need) return SPA_ERR_WORKSPACE;
+      const size_t tsh = (size_t)pr->num_tokens * pl.splits * pr->num_heads;
+      p.ws_o = static_cast<float*>(ws);
+      p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                          align256(tsh * pr->head_dim * sizeof(float)));
+      p.decode = 1;
+      merge = true;
+    }
   } else {
     p.n_splits = 1;
     p.cols_per_split = C > 0 ? C : 1;
@@ -175,11 +234,12 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   const long long items = (long long)pr->num_tokens * p.n_groups * p.n_splits;
   if (items > 0x7fffffffLL) return SPA_ERR_UNSUPPORTED;
   p.n_items = (int)items;
-  const int grid = (int)(items < sms ? items : sms);
+  // clustered: one item per CTA; otherwise a persistent grid of at most one CTA per SM
+  const int grid = p.cluster > 1 ? (int)items : (int)(items < sms ? items : sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = spa::launch_attn(p, grid, fp8, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-  if (decode) {
+  if (merge) {
     e = spa::launch_merge(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   }
@@ -187,6 +247,23 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
 }
 
 }  // namespace
+
+namespace spa {
+size_t decode_partials_bytes(const spa_problem_t* prob) {
+  if (!prob || prob->num_tokens < 0 || prob->num_heads < 1 || prob->head_dim < 1) return 0;
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != SPA_OK) return 0;
+  int splits = 1, cols = 1;
+  decode_plan_ws(prob, sms, &splits, &cols);
+  return workspace_bytes(prob, splits);
+}
+
+int decode_with_partials(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                         const spa_problem_t* prob, void* out, void* ws, size_t ws_bytes,
+                         void* stream) {
+  return run(q, win, cmp, prob, out, ws, ws_bytes, stream, true, false, true);
+}
+}  // namespace spa
 
 extern "C" {
 
@@ -204,9 +281,8 @@ size_t sparse_attn_paged_decode_workspace_size(const spa_problem_t* prob) {
   if (!prob || prob->num_tokens < 0 || prob->num_heads < 1 || prob->head_dim < 1) return 0;
   int dev = 0, sms = 0;
   if (current_device(&dev, &sms) != SPA_OK) return 0;
-  int splits = 1, cols = 1;
-  decode_plan(prob, sms, &splits, &cols);
-  return workspace_bytes(prob, splits);
+  const DecodePlan pl = decode_plan(prob, dev, sms);
+  return (pl.cluster > 1 || pl.splits == 1) ? 0 : workspace_bytes(prob, pl.splits);
 }
 
 int sparse_attn_paged_decode(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,

@@ -63,7 +63,7 @@ constexpr int kBarOff = kCntOff + 64;
 enum {
   B_FULL = 0, B_EMPTY = 4, B_QFULL = 8, B_QEMPTY = 9, B_SFULL = 10, B_SEMPTY = 12,
   B_PFULL = 14, B_PVDONE = 15, B_OFREE = 16, B_TIFULL = 17, B_TIEMPTY = 21, B_RED = 25,
-  B_DRAIN = 27, B_COUNT = 28
+  B_DRAIN = 27, B_READY = 28, B_RECV = 29, B_RECVML = 30, B_COUNT = 31
 };
 constexpr int kMiscOff = kBarOff + B_COUNT * 8;             // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;            // + slack to align the base to 1 KB
@@ -149,6 +149,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// The same for phases completed by arrivals from the CTAs of the cluster (parity 0: one use).
+__device__ __forceinline__ bool warp_wait_cl(uint32_t bar, volatile int* abort_flag) {
+  const bool ok = mbar_wait_cluster(bar, 0, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // A wait that must end even when the CTA is aborting (drain before releasing TMEM).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -181,6 +187,11 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
   lo = e4m3x2(a - h.x, b - h.y);
 }
 
+// Two fp32 values -> packed bf16x2 (round to nearest even), first value in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
@@ -228,6 +239,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       mbar_init(BAR(B_TIEMPTY + i), 5);
     }
     mbar_init(BAR(B_DRAIN), 1);
+    // cluster merge: one "ring idle" arrival from every CTA; the bulk copies of every CTA's
+    // slice and (m, l) complete the receive barrier's transaction count, armed here
+    mbar_init(BAR(B_READY), p.cluster > 1 ? p.cluster : 1);
+    mbar_init(BAR(B_RECV), 1);
+    mbar_init(BAR(B_RECVML), 1);
+    if (p.cluster > 1) {
+      mbar_arrive_expect_tx(BAR(B_RECV), (uint32_t)(p.D * 128));
+      mbar_arrive_expect_tx(BAR(B_RECVML), (uint32_t)(p.cluster * 512));
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -236,6 +256,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kMiscOff);
+  // A cluster's CTAs touch one another's shared memory only after all of them have started and
+  // initialised their barriers: every thread arrives here and waits before its first remote access.
+  const bool clustered = p.cluster > 1;
+  bool cl_started = !clustered;
+  bool recv_ok = false;  // thread 0: the cluster merge's receive barrier was seen complete
+  if (clustered) cluster_arrive();
 
   const int D = p.D;
   const int P16 = D * M::kElt / 16;       // 16-byte pieces per K (or V) row
@@ -309,12 +335,18 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       }
       const int n_tiles = (n + 127) >> 7;
       const int n_ti = n_tiles > 0 ? n_tiles : 1;
-      if (n > 0) {
-        // Q of this token and head group
+      // Q of this token and head group.  Every item takes one turn of the buffer, also one
+      // without columns.  The first item's bf16 q is loaded by the softmax warps at kernel
+      // start, in parallel with this walk of the page tables.
+      if (!kFp8 && item == (int)blockIdx.x) {
+        q_ph ^= 1;
+      } else {
         mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
         q_ph ^= 1;
-        const uint32_t qs = sb + kQOff;
-        if (!kFp8) {
+        if (n == 0) {
+          mbar_arrive(BAR(B_QFULL));
+        } else if (!kFp8) {
+          const uint32_t qs = sb + kQOff;
           // bf16: [atom][64 heads][128 B], heads beyond H zero-filled
           for (int it = 0; it < 4 * n_atoms; ++it) {
             const int h = (it & 3) * 16 + r0;
@@ -475,11 +507,14 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         mbar_arrive(BAR(B_TIEMPTY + tik));
         if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
         if (item < 0) break;
-        if (n == 0) continue;
         const bool first = flags & kFirst, last = flags & kLast;
         if (first) {
           if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;
           q_ph ^= 1;
+        }
+        if (n == 0) {  // an item without columns: hand the Q buffer back untouched
+          mma_commit(BAR(B_QEMPTY));
+          continue;
         }
         if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) break;
         s_ph ^= 1u << sbuf;
@@ -578,6 +613,23 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
     float p_scale = 1.f;
     int t = 0, g = 0, s = 0;
     bool had = false;
+    if (!kFp8) {
+      // q of this CTA's first item (bf16: [atom][64 heads][128 B], heads beyond H zero-filled),
+      // loaded here while the gather warps walk the page tables; the buffer starts out free
+      const int tg0 = (int)blockIdx.x / p.n_splits;
+      const int g0 = tg0 % p.n_groups, t0 = tg0 / p.n_groups;
+      const int jq = tid & 7, rq = tid >> 3;
+      const uint32_t qs = sb + kQOff;
+      for (int it = 0; it < 4 * n_atoms; ++it) {
+        const int h = (it & 3) * 16 + rq;
+        const int a = it >> 2;
+        const int hg = g0 * 64 + h;
+        const bool okq = hg < p.H;
+        const uint8_t* src = p.q + (((size_t)t0 * p.H + (okq ? hg : 0)) * D) * 2 + a * 128 + jq * 16;
+        cp_async_16(qs + a * M::kQAtom + h * 128 + ((jq ^ (h & 7)) << 4), src, okq ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(BAR(B_QFULL));
+    }
     for (;;) {
       if (!warp_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
       const int item = ti[tik].item;
@@ -738,6 +790,153 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         tc_fence_before();
         mbar_arrive(BAR(B_PFULL));
       }
+      if (last && clustered) {
+        // ---- split-K merge inside the cluster (one item per CTA; rank == split index) ----
+        // Every CTA sends CTA k its (m, l) per head and the rows [k*dpo, (k+1)*dpo) of its
+        // unnormalised O^T in bf16; CTA k weights split s by 2^(m_s - M) / sum_j 2^(m_j - M) l_j
+        // and stores the sum.  Transfers are bulk copies between the shared memories of the
+        // cluster; the (m, l) copies go first so the weights are ready when the rows land.
+        // No early exit until the last named barrier: all four softmax warps must reach each of
+        // them; a failed wait (which sets the abort flag) only skips work.
+        const int S = p.cluster;
+        const int dpo = D / S;
+        float L0 = 0.f, L1 = 0.f;
+        bool ok = true;
+        if (had) {
+          ok = warp_wait(BAR(B_PVDONE), pv_ph, abort_flag);
+          pv_ph ^= 1;
+          tc_fence_after();
+          float* rr = red + rb * 256;
+          rr[warp * 64 + lane] = l0;
+          rr[warp * 64 + 32 + lane] = l1;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_RED + rb));
+          ok = ok && warp_wait(BAR(B_RED + rb), (red_ph >> rb) & 1u, abort_flag);
+          red_ph ^= 1u << rb;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            L0 += rr[w * 64 + lane];
+            L1 += rr[w * 64 + 32 + lane];
+          }
+          rb ^= 1;
+        }
+        cluster_wait();
+        cl_started = true;
+        const uint32_t rank = cluster_ctarank();
+        // this CTA's ring is idle from here on: tell every CTA of the cluster
+        if (ok && tid < S) mbar_arrive_cluster(mapa_cluster(BAR(B_READY), (uint32_t)tid));
+        if (warp == 0) {
+          // O carries the probability scale p (e4m3; 1 for bf16) and l does not: sending
+          // (m - log2 p, l * p) makes 2^(m' - M') = 2^(m - M') / p and leaves 2^(m' - M') l'
+          // unchanged, so the merge below needs no separate scale
+          const float lp = __log2f(p_scale);
+          float2* mlo = reinterpret_cast<float2*>(sm + kPOff);
+          mlo[lane] = make_float2(had ? m0 - lp : -INFINITY, L0 * p_scale);
+          mlo[32 + lane] = make_float2(had ? m1 - lp : -INFINITY, L1 * p_scale);
+        }
+        // stage O^T as bf16 [D rows][64 heads] in the Q buffer, 16-byte chunk c of row d at
+        // chunk position c ^ (d & 7)
+#pragma unroll 1
+        for (int i = 0; i < n_mt; ++i) {
+          const int d = i * 128 + tid;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            float o[32];
+            tmem_ld32(lane_base + M::kOCol + i * 64 + hf * 32, o);
+            tmem_wait_ld();
+            if (d < D) {
+              uint8_t* row = sm + kQOff + (size_t)d * 128;
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 u;
+                u.x = pack_bf16x2(o[8 * q4 + 0], o[8 * q4 + 1]);
+                u.y = pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]);
+                u.z = pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]);
+                u.w = pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]);
+                *reinterpret_cast<uint4*>(row + (((hf * 4 + q4) ^ (d & 7)) << 4)) = u;
+              }
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        // lane k of warp 0 sends to CTA k: (m, l) into its ML area, then the row slice into its
+        // ring at [rank][dpo rows][128 B]
+        if (warp == 0 && lane < S && ok && !*abort_flag) {
+          if (mbar_wait_cluster(BAR(B_READY), 0, abort_flag)) {
+            const uint32_t k = (uint32_t)lane;
+            bulk_copy_cluster(mapa_cluster(sb + kRingOff + D * 128 + rank * 512, k), sb + kPOff, 512,
+                              mapa_cluster(BAR(B_RECVML), k));
+            bulk_copy_cluster(mapa_cluster(sb + kRingOff + rank * dpo * 128, k),
+                              sb + kQOff + (uint32_t)(k * dpo * 128), dpo * 128,
+                              mapa_cluster(BAR(B_RECV), k));
+          }
+        }
+        // merge weights per (split, head), computed while the rows are in flight
+        ok = ok && warp_wait(BAR(B_RECVML), 0, abort_flag);
+        const float2* mlr = reinterpret_cast<const float2*>(sm + kRingOff + D * 128);
+        float* wk = reinterpret_cast<float*>(sm + kPOff + 1024);
+        if (ok && tid < 64) {
+          float m[16], l[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 v = k < S ? mlr[k * 64 + tid] : make_float2(-INFINITY, 0.f);
+            m[k] = v.x;
+            l[k] = v.y;
+          }
+          float Mh = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) Mh = fmaxf(Mh, m[k]);
+          float tot = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            m[k] = (m[k] != -INFINITY) ? fast_exp2(m[k] - Mh) : 0.f;
+            tot += m[k] * l[k];
+          }
+          const float it = tot > 0.f ? 1.f / tot : 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (k < S) wk[k * 64 + tid] = m[k] * it;
+        }
+        ok = ok && warp_wait(BAR(B_RECV), 0, abort_flag);
+        if (ok && tid == 0) recv_ok = true;
+        named_bar_sync(1, 128);
+        if (!ok || *abort_flag) break;
+        {
+          // out rows [rank*dpo, (rank+1)*dpo) of every head: sum_s w[s][h] * O_s[row][h]
+          const int Hg = min(64, p.H - g * 64);
+          const uint8_t* rv = sm + kRingOff;
+          __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                              ((size_t)t * p.H + g * 64) * D + rank * dpo;
+#pragma unroll 1
+          for (int idx = tid; idx < dpo * 8; idx += 128) {
+            const int dl = idx % dpo, c = idx / dpo;   // row, chunk of 8 heads
+            const int pos = (c ^ ((rank * dpo + dl) & 7)) << 4;
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 4
+            for (int k = 0; k < S; ++k) {
+              const uint4 u = *reinterpret_cast<const uint4*>(rv + (size_t)(k * dpo + dl) * 128 + pos);
+              const float4 wa = *reinterpret_cast<const float4*>(wk + k * 64 + 8 * c);
+              const float4 wb = *reinterpret_cast<const float4*>(wk + k * 64 + 8 * c + 4);
+              // a split without columns has weight 0 and whatever its TMEM held: skip it exactly
+              acc[0] += wa.x != 0.f ? wa.x * bf16_lo(u.x) : 0.f;
+              acc[1] += wa.y != 0.f ? wa.y * bf16_hi(u.x) : 0.f;
+              acc[2] += wa.z != 0.f ? wa.z * bf16_lo(u.y) : 0.f;
+              acc[3] += wa.w != 0.f ? wa.w * bf16_hi(u.y) : 0.f;
+              acc[4] += wb.x != 0.f ? wb.x * bf16_lo(u.z) : 0.f;
+              acc[5] += wb.y != 0.f ? wb.y * bf16_hi(u.z) : 0.f;
+              acc[6] += wb.z != 0.f ? wb.z * bf16_lo(u.w) : 0.f;
+              acc[7] += wb.w != 0.f ? wb.w * bf16_hi(u.w) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (8 * c + e < Hg) ob[(size_t)(8 * c + e) * D + dl] = __float2bfloat16_rn(acc[e]);
+          }
+        }
+        continue;
+      }
       if (last) {
         const int Hg = min(64, p.H - g * 64);
         if (!had) {
@@ -819,6 +1018,17 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       }
     }
   }
+  if (clustered) {
+    // no CTA leaves while a peer may still read or write its shared memory
+    if (!cl_started) cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+    // after a failed merge, copies from peers may still be landing here: let them finish
+    if (threadIdx.x == 0 && !recv_ok) {
+      mbar_wait_drain(BAR(B_RECVML), 0);
+      mbar_wait_drain(BAR(B_RECV), 0);
+    }
+  }
 #undef BAR
   tc_fence_before();
   __syncthreads();
@@ -894,19 +1104,55 @@ __global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ c
 }
 
 cudaError_t prepare_attn_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, cfg::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              cfg::kSmemBytes);
+  for (int f = 0; f < 2; ++f) {
+    const void* k = f ? reinterpret_cast<const void*>(attn_kernel<true>)
+                      : reinterpret_cast<const void*>(attn_kernel<false>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // clusters of up to 16 CTAs (the split-K merge through distributed shared memory)
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+namespace {
+cudaLaunchConfig_t attn_config(int grid, int cluster, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3((unsigned)grid, 1, 1);
+  c.blockDim = dim3(cfg::kThreads, 1, 1);
+  c.dynamicSmemBytes = cfg::kSmemBytes;
+  c.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)(cluster > 1 ? cluster : 1);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  c.attrs = attr;
+  c.numAttrs = cluster > 1 ? 1 : 0;
+  return c;
+}
+}  // namespace
+
+int attn_max_active_clusters(int cluster, bool fp8) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c = attn_config(cluster, cluster, nullptr, attr);
+  int n = 0;
+  const void* k = fp8 ? reinterpret_cast<const void*>(attn_kernel<true>)
+                      : reinterpret_cast<const void*>(attn_kernel<false>);
+  if (cudaOccupancyMaxActiveClusters(&n, k, &c) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t stream) {
-  if (fp8)
-    attn_kernel<true><<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
-  else
-    attn_kernel<false><<<grid, cfg::kThreads, cfg::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr);
+  if (fp8) return cudaLaunchKernelEx(&c, attn_kernel<true>, p);
+  return cudaLaunchKernelEx(&c, attn_kernel<false>, p);
 }
 
 int merge_max_splits() { return kMergeMaxSplits; }

@@ -19,7 +19,9 @@ struct AttnParams {
   int cols_per_split;   // raw columns per split
   int n_items;          // T * n_groups * n_splits
   float scale_log2;     // softmax scale * log2(e)
-  int decode;
+  int decode;           // 1: write split partials to ws_o / ws_lse for the merge kernel
+  int cluster;          // > 1: the n_splits CTAs of one (token, head group) form a thread-block
+                        // cluster and merge their partials through distributed shared memory
 };
 
 // Kernel launch configuration.
@@ -28,10 +30,20 @@ int attn_smem_bytes();
 constexpr int kMaxColumns = 1024;     // window + top-k columns per query
 
 cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t stream);
+// Largest number of `cluster`-CTA clusters of the attention kernel that can run at once
+// (0 when clusters of that size cannot be launched on this device).
+int attn_max_active_clusters(int cluster, bool fp8);
 int merge_max_splits();
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_resolve_dump(const ResolveArgs& a, int32_t* cols, cudaStream_t stream);
 cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)
 cudaError_t read_and_clear_error_word(int* value);
+
+// Decode through split-K partials in a caller-given buffer and the merge kernel, whatever the
+// usual plan would be (the path of the no-alloc entry point), and the bytes it needs.
+size_t decode_partials_bytes(const spa_problem_t* prob);
+int decode_with_partials(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                         const spa_problem_t* prob, void* out, void* ws, size_t ws_bytes,
+                         void* stream);
 
 }  // namespace spa

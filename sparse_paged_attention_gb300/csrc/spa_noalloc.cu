@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "sparse_attn_paged.h"
+#include "spa_launch.h"
 
 namespace {
 
@@ -46,9 +47,9 @@ extern "C" int sparse_attn_paged_decode_noalloc(const void* q, const spa_pool_t*
                                                 void* out, void* stream) {
   if (!prob) return SPA_ERR_NULL;
   // The partials of this problem must fit the built-in array; no larger buffer can be had here.
-  if (sparse_attn_paged_decode_workspace_size(prob) > kScratchBytes) return SPA_ERR_WORKSPACE;
+  if (spa::decode_partials_bytes(prob) > kScratchBytes) return SPA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);
   if (st != SPA_OK) return st;
-  return sparse_attn_paged_decode(q, win, cmp, prob, out, scratch, kScratchBytes, stream);
+  return spa::decode_with_partials(q, win, cmp, prob, out, scratch, kScratchBytes, stream);
 }
