@@ -133,16 +133,23 @@ void fill_resolve(spa::ResolveArgs& a, const spa_pool_t* win, const spa_pool_t* 
 //    kernel (decode_plan_ws).
 struct DecodePlan {
   int splits, cols, cluster;  // cluster == 0 with splits > 1: workspace + merge kernel
+  int gh;                     // heads per group (64, or 32 to give one query more CTAs)
 };
 
 void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols);
 
 DecodePlan decode_plan(const spa_problem_t* pr, int dev, int sms) {
   const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
-  const long long groups = (pr->num_heads + 63) / 64;
-  const long long base = (long long)pr->num_tokens * groups;
-  DecodePlan pl{1, C, 0};
-  if (base <= 0 || 2 * base >= sms) return pl;
+  const long long T = pr->num_tokens;
+  DecodePlan pl{1, C, 0, 64};
+  // groups of 32 heads halve what each CTA merges; worth it when 16-way splits still fit
+  if (pr->num_heads <= 32 || T * ((pr->num_heads + 31) / 32) * 16 <= sms) pl.gh = 32;
+  const long long groups = (pr->num_heads + pl.gh - 1) / pl.gh;
+  const long long base = T * groups;
+  if (base <= 0 || 2 * base >= sms) {
+    pl.gh = 64;
+    return pl;
+  }
   int S = 16;
   while (S > 1 && ((long long)S * base > sms || (C + S - 1) / S < 16)) S >>= 1;
   while (S > 1 && max_active_clusters(dev, S) < base) S >>= 1;
@@ -152,6 +159,7 @@ DecodePlan decode_plan(const spa_problem_t* pr, int dev, int sms) {
     pl.cluster = S;
     return pl;
   }
+  pl.gh = 64;
   if (max_active_clusters(dev, 2) >= 1) return pl;  // clusters work; one split is the best fit
   decode_plan_ws(pr, sms, &pl.splits, &pl.cols);
   return pl;
@@ -201,6 +209,7 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   p.out = static_cast<uint8_t*>(out);
   p.H = pr->num_heads;
   p.D = pr->head_dim;
+  p.gh = 64;
   p.n_groups = (pr->num_heads + 63) / 64;
   p.scale_log2 = pr->scale * 1.4426950408889634f;
   const int C = pr->window + pr->topk;
@@ -209,8 +218,11 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
     DecodePlan pl = decode_plan(pr, dev, sms);
     if (force_partials && (pl.cluster > 1 || pl.splits == 1)) {
       pl.cluster = 0;
+      pl.gh = 64;
       decode_plan_ws(pr, sms, &pl.splits, &pl.cols);
     }
+    p.gh = pl.gh;
+    p.n_groups = (pr->num_heads + pl.gh - 1) / pl.gh;
     p.n_splits = pl.splits;
     p.cols_per_split = pl.cols;
     p.cluster = pl.cluster;

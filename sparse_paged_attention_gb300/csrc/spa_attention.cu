@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
     mbar_init(BAR(B_RECV), 1);
     mbar_init(BAR(B_RECVML), 1);
     if (p.cluster > 1) {
-      mbar_arrive_expect_tx(BAR(B_RECV), (uint32_t)(p.D * 128));
-      mbar_arrive_expect_tx(BAR(B_RECVML), (uint32_t)(p.cluster * 512));
+      mbar_arrive_expect_tx(BAR(B_RECV), (uint32_t)(p.D * p.gh * 2));
+      mbar_arrive_expect_tx(BAR(B_RECVML), (uint32_t)(p.cluster * p.gh * 8));
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
           for (int it = 0; it < 4 * n_atoms; ++it) {
             const int h = (it & 3) * 16 + r0;
             const int a = it >> 2;
-            const int hg = g * 64 + h;
-            const bool ok = hg < p.H;
+            const int hg = g * p.gh + h;
+            const bool ok = h < p.gh && hg < p.H;
             const uint8_t* src = p.q + (((size_t)t * p.H + (ok ? hg : 0)) * D) * 2 + a * 128 + jj * 16;
             cp_async_16(qs + a * M::kQAtom + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
           }
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
               const int h = (it & 3) * 16 + r0;
               const int a = it >> 2;
               const int piece = a * 8 + jj;      // 16 head_dim values
-              const int hg = g * 64 + h;
-              const bool ok = hg < p.H && piece < P16;
+              const int hg = g * p.gh + h;
+              const bool ok = h < p.gh && hg < p.H && piece < P16;
               uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
               if (ok) {
                 const uint4* src = reinterpret_cast<const uint4*>(
@@ -457,7 +457,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         const int nj = min(128, n - j * 128);
         const int pv_step = kFp8 ? 32 : 16;
         const int v_rows = (nj + pv_step - 1) / pv_step * pv_step;
-        for (int half = 0; half < 2; ++half) {      // K rows, then V rows
+        // A tile of at most 64 columns is packed: K in rows 0..63 and V in rows 64..127 of the
+        // same slots, so V lands with K (the S MMA's rows past 63 are masked columns).
+        const bool packed = nj <= 64;
+        const int kmax_v = packed ? (v_rows + 15) >> 4 : 0;
+        for (int half = 0; half < (packed ? 1 : 2); ++half) {  // K rows, then V rows
           const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
           for (int kc = 0; kc < n_chunks; ++kc) {
             mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
@@ -471,6 +475,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
                 const uint32_t sz = src[k] ? 16u : 0u;
                 if (a0) cp_async_16(d0 + k * 2048, sp, sz);
                 if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (k < kmax_v) {
+                const uint8_t* sp = src[k] ? src[k] + so + D * M::kElt : p.q;
+                const uint32_t sz = src[k] ? 16u : 0u;
+                if (a0) cp_async_16(d0 + (4 + k) * 2048, sp, sz);
+                if (a1) cp_async_16(d0 + kAtomBytes + (4 + k) * 2048, sp + 128, sz);
               }
             }
             cp_async_arrive_noinc(BAR(B_FULL + ring));
@@ -522,6 +535,9 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         tc_fence_after();
         bool ok = true;
         const uint32_t dS = tmem + sbuf * M::kSCols;
+        const bool packed = n <= 64;   // K and V share the slots (see the gather warps)
+        const int ring0 = ring;
+        const uint32_t ring_ph0 = ring_ph;
         for (int kc = 0; kc < n_chunks; ++kc) {
           if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
           fence_proxy_async_smem();
@@ -541,11 +557,16 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
                 mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
             }
           }
-          mma_commit(BAR(B_EMPTY + ring));
+          if (!packed) mma_commit(BAR(B_EMPTY + ring));
           if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
         }
         if (!ok) break;
         mma_commit(BAR(B_SFULL + sbuf));
+        if (packed) {  // PV reads the same slots
+          ring = ring0;
+          ring_ph = ring_ph0;
+        }
+        const uint32_t v_off = packed ? 64u * 128u : 0u;
         if (last) mma_commit(BAR(B_QEMPTY));
         sbuf ^= 1;
         if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) break;
@@ -566,7 +587,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
             const uint32_t dO = tmem + M::kOCol + vc * 64;
             const int nk = (n + 15) >> 4;
             for (int kk = 0; kk < nk; ++kk) {
-              const uint64_t da = sdesc(slot + kk * 2048, kAtomBytes, 1024);
+              const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
               const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
               mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
             }
@@ -579,7 +600,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
               if (mt >= n_mt) break;
               const uint32_t dO = tmem + M::kOCol + mt * 64;
               for (int kk = 0; kk < nk; ++kk) {
-                const uint64_t da = sdesc(slot + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
+                const uint64_t da = sdesc(slot + v_off + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
                 const uint64_t dh = sdesc64(pbase + kk * 2048, 8192, 512);
                 const uint64_t dl = sdesc64(pbase + 8192 + kk * 2048, 8192, 512);
                 mma_f8(dO, da, dh, idO, (first && kk == 0) ? 0u : 1u);
@@ -623,8 +644,8 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       for (int it = 0; it < 4 * n_atoms; ++it) {
         const int h = (it & 3) * 16 + rq;
         const int a = it >> 2;
-        const int hg = g0 * 64 + h;
-        const bool okq = hg < p.H;
+        const int hg = g0 * p.gh + h;
+        const bool okq = h < p.gh && hg < p.H;
         const uint8_t* src = p.q + (((size_t)t0 * p.H + (okq ? hg : 0)) * D) * 2 + a * 128 + jq * 16;
         cp_async_16(qs + a * M::kQAtom + h * 128 + ((jq ^ (h & 7)) << 4), src, okq ? 16u : 0u);
       }
@@ -825,27 +846,35 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         const uint32_t rank = cluster_ctarank();
         // this CTA's ring is idle from here on: tell every CTA of the cluster
         if (ok && tid < S) mbar_arrive_cluster(mapa_cluster(BAR(B_READY), (uint32_t)tid));
+        // (m - log2 p, l * p) per head: O carries the probability scale p (e4m3; 1 for bf16)
+        // and l does not, so 2^(m' - M') = 2^(m - M') / p while 2^(m' - M') l' is unchanged
+        const int gh = p.gh;
+        const int rb_bytes = gh * 2;          // one staged O^T row: gh bf16 heads
+        const int cpr = gh >> 3;              // 16-byte chunks per row
+        const int ml_bytes = gh * 8;
         if (warp == 0) {
-          // O carries the probability scale p (e4m3; 1 for bf16) and l does not: sending
-          // (m - log2 p, l * p) makes 2^(m' - M') = 2^(m - M') / p and leaves 2^(m' - M') l'
-          // unchanged, so the merge below needs no separate scale
           const float lp = __log2f(p_scale);
           float2* mlo = reinterpret_cast<float2*>(sm + kPOff);
-          mlo[lane] = make_float2(had ? m0 - lp : -INFINITY, L0 * p_scale);
-          mlo[32 + lane] = make_float2(had ? m1 - lp : -INFINITY, L1 * p_scale);
+          if (lane < gh) mlo[lane] = make_float2(had ? m0 - lp : -INFINITY, L0 * p_scale);
+          if (32 + lane < gh) mlo[32 + lane] = make_float2(had ? m1 - lp : -INFINITY, L1 * p_scale);
         }
-        // stage O^T as bf16 [D rows][64 heads] in the Q buffer, 16-byte chunk c of row d at
-        // chunk position c ^ (d & 7)
+        // stage O^T as bf16 [D rows][gh heads] in the Q buffer (zeros for a split without
+        // columns, whose TMEM was never written), chunk c of row d at position c ^ (d & (cpr-1))
 #pragma unroll 1
         for (int i = 0; i < n_mt; ++i) {
           const int d = i * 128 + tid;
 #pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
+          for (int hf = 0; hf < (gh >> 5); ++hf) {
             float o[32];
-            tmem_ld32(lane_base + M::kOCol + i * 64 + hf * 32, o);
-            tmem_wait_ld();
+            if (had) {
+              tmem_ld32(lane_base + M::kOCol + i * 64 + hf * 32, o);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = 0.f;
+            }
             if (d < D) {
-              uint8_t* row = sm + kQOff + (size_t)d * 128;
+              uint8_t* row = sm + kQOff + (size_t)d * rb_bytes;
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
                 uint4 u;
@@ -853,34 +882,38 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
                 u.y = pack_bf16x2(o[8 * q4 + 2], o[8 * q4 + 3]);
                 u.z = pack_bf16x2(o[8 * q4 + 4], o[8 * q4 + 5]);
                 u.w = pack_bf16x2(o[8 * q4 + 6], o[8 * q4 + 7]);
-                *reinterpret_cast<uint4*>(row + (((hf * 4 + q4) ^ (d & 7)) << 4)) = u;
+                *reinterpret_cast<uint4*>(row + (((hf * 4 + q4) ^ (d & (cpr - 1))) << 4)) = u;
               }
             }
           }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        // lane k of warp 0 sends to CTA k: (m, l) into its ML area, then the row slice into its
-        // ring at [rank][dpo rows][128 B]
-        if (warp == 0 && lane < S && ok && !*abort_flag) {
-          if (mbar_wait_cluster(BAR(B_READY), 0, abort_flag)) {
-            const uint32_t k = (uint32_t)lane;
-            bulk_copy_cluster(mapa_cluster(sb + kRingOff + D * 128 + rank * 512, k), sb + kPOff, 512,
+        // lane k of warp 0 sends to CTA k: first every (m, l) block, then the row slices, so the
+        // small copies are not queued behind the large ones
+        const uint32_t recv_ml = sb + kRingOff + (uint32_t)(D * rb_bytes);
+        const bool send = ok && __shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0) != 0;
+        if (warp == 0 && lane < S && send) {   // (the same lanes on both sides of the warp sync)
+          const uint32_t k = (uint32_t)lane;
+          const bool go = mbar_wait_cluster(BAR(B_READY), 0, abort_flag);
+          if (go)
+            bulk_copy_cluster(mapa_cluster(recv_ml + rank * ml_bytes, k), sb + kPOff, ml_bytes,
                               mapa_cluster(BAR(B_RECVML), k));
-            bulk_copy_cluster(mapa_cluster(sb + kRingOff + rank * dpo * 128, k),
-                              sb + kQOff + (uint32_t)(k * dpo * 128), dpo * 128,
+          __syncwarp((1u << S) - 1u);
+          if (go)
+            bulk_copy_cluster(mapa_cluster(sb + kRingOff + rank * dpo * rb_bytes, k),
+                              sb + kQOff + (uint32_t)(k * dpo * rb_bytes), dpo * rb_bytes,
                               mapa_cluster(BAR(B_RECV), k));
-          }
         }
         // merge weights per (split, head), computed while the rows are in flight
         ok = ok && warp_wait(BAR(B_RECVML), 0, abort_flag);
-        const float2* mlr = reinterpret_cast<const float2*>(sm + kRingOff + D * 128);
+        const float2* mlr = reinterpret_cast<const float2*>(sm + kRingOff + D * rb_bytes);
         float* wk = reinterpret_cast<float*>(sm + kPOff + 1024);
-        if (ok && tid < 64) {
+        if (ok && tid < gh) {
           float m[16], l[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float2 v = k < S ? mlr[k * 64 + tid] : make_float2(-INFINITY, 0.f);
+            const float2 v = k < S ? mlr[k * gh + tid] : make_float2(-INFINITY, 0.f);
             m[k] = v.x;
             l[k] = v.y;
           }
@@ -904,31 +937,33 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         if (!ok || *abort_flag) break;
         {
           // out rows [rank*dpo, (rank+1)*dpo) of every head: sum_s w[s][h] * O_s[row][h]
-          const int Hg = min(64, p.H - g * 64);
+          // (a split without columns sent zeros with weight 0)
+          const int Hg = min(gh, p.H - g * gh);
           const uint8_t* rv = sm + kRingOff;
           __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                              ((size_t)t * p.H + g * 64) * D + rank * dpo;
+                              ((size_t)t * p.H + g * gh) * D + rank * dpo;
 #pragma unroll 1
-          for (int idx = tid; idx < dpo * 8; idx += 128) {
+          for (int idx = tid; idx < dpo * cpr; idx += 128) {
             const int dl = idx % dpo, c = idx / dpo;   // row, chunk of 8 heads
-            const int pos = (c ^ ((rank * dpo + dl) & 7)) << 4;
+            const int pos = (c ^ ((rank * dpo + dl) & (cpr - 1))) << 4;
+            const uint8_t* src = rv + (size_t)dl * rb_bytes + pos;
+            const float* wc = wk + 8 * c;
             float acc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll 4
             for (int k = 0; k < S; ++k) {
-              const uint4 u = *reinterpret_cast<const uint4*>(rv + (size_t)(k * dpo + dl) * 128 + pos);
-              const float4 wa = *reinterpret_cast<const float4*>(wk + k * 64 + 8 * c);
-              const float4 wb = *reinterpret_cast<const float4*>(wk + k * 64 + 8 * c + 4);
-              // a split without columns has weight 0 and whatever its TMEM held: skip it exactly
-              acc[0] += wa.x != 0.f ? wa.x * bf16_lo(u.x) : 0.f;
-              acc[1] += wa.y != 0.f ? wa.y * bf16_hi(u.x) : 0.f;
-              acc[2] += wa.z != 0.f ? wa.z * bf16_lo(u.y) : 0.f;
-              acc[3] += wa.w != 0.f ? wa.w * bf16_hi(u.y) : 0.f;
-              acc[4] += wb.x != 0.f ? wb.x * bf16_lo(u.z) : 0.f;
-              acc[5] += wb.y != 0.f ? wb.y * bf16_hi(u.z) : 0.f;
-              acc[6] += wb.z != 0.f ? wb.z * bf16_lo(u.w) : 0.f;
-              acc[7] += wb.w != 0.f ? wb.w * bf16_hi(u.w) : 0.f;
+              const uint4 u = *reinterpret_cast<const uint4*>(src + (size_t)k * dpo * rb_bytes);
+              const float4 wa = *reinterpret_cast<const float4*>(wc + k * 64);
+              const float4 wb = *reinterpret_cast<const float4*>(wc + k * 64 + 4);
+              acc[0] = fmaf(wa.x, bf16_lo(u.x), acc[0]);
+              acc[1] = fmaf(wa.y, bf16_hi(u.x), acc[1]);
+              acc[2] = fmaf(wa.z, bf16_lo(u.y), acc[2]);
+              acc[3] = fmaf(wa.w, bf16_hi(u.y), acc[3]);
+              acc[4] = fmaf(wb.x, bf16_lo(u.z), acc[4]);
+              acc[5] = fmaf(wb.y, bf16_hi(u.z), acc[5]);
+              acc[6] = fmaf(wb.z, bf16_lo(u.w), acc[6]);
+              acc[7] = fmaf(wb.w, bf16_hi(u.w), acc[7]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -938,15 +973,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         continue;
       }
       if (last) {
-        const int Hg = min(64, p.H - g * 64);
+        const int Hg = min(p.gh, p.H - g * p.gh);
         if (!had) {
           // no column at all: out = 0 (prefill) or an empty partial (decode)
           if (p.decode) {
-            const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * 64;
+            const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * p.gh;
             for (int i = tid; i < Hg * D; i += 128) p.ws_o[pb * D + i] = 0.f;
             if (tid < Hg) p.ws_lse[pb + tid] = -INFINITY;
           } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)t * p.H + g * 64) * D;
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)t * p.H + g * p.gh) * D;
             for (int i = tid; i < Hg * D; i += 128) o[i] = __float2bfloat16_rn(0.f);
           }
           continue;
@@ -973,7 +1008,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         arow[32 + lane] = 1.f / (L1 * p_scale);
         __syncwarp();
         if (p.decode && warp == 0) {
-          const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * 64;
+          const size_t pb = ((size_t)t * p.n_splits + s) * p.H + g * p.gh;
           if (lane < Hg) p.ws_lse[pb + lane] = m0 + __log2f(L0);
           if (32 + lane < Hg) p.ws_lse[pb + 32 + lane] = m1 + __log2f(L1);
         }
@@ -982,7 +1017,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
           float inv[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) inv[k] = arow[hf * 32 + k];
-          const size_t row0 = (size_t)t * p.H + g * 64 + hf * 32;  // first head of this half
+          const size_t row0 = (size_t)t * p.H + g * p.gh + hf * 32;  // first head of this half
           const int nh = min(32, Hg - hf * 32);                     // heads of this half present
 #pragma unroll 1
           for (int i = 0; i < n_mt; ++i) {
@@ -992,7 +1027,7 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
             tmem_wait_ld();
             if (d < D) {
               if (p.decode) {
-                float* wo = p.ws_o + (((size_t)t * p.n_splits + s) * p.H + g * 64 + hf * 32) * D + d;
+                float* wo = p.ws_o + (((size_t)t * p.n_splits + s) * p.H + g * p.gh + hf * 32) * D + d;
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
                   if (k < nh) wo[(uint32_t)(k * D)] = o[k] * inv[k];

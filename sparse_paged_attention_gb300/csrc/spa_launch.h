@@ -14,7 +14,8 @@ struct AttnParams {
   float* ws_o;          // decode partials [T][S][H][D], each normalised by its own denominator
   float* ws_lse;        // decode partial log-sum-exp, base 2, [T][S][H]
   int H, D;
-  int n_groups;         // ceil(H / 64): heads are processed 64 at a time
+  int gh;               // heads per group: 64, or 32 when a decode needs more CTAs per query
+  int n_groups;         // ceil(H / gh): the MMAs always see 64 head rows, the ones past gh zero
   int n_splits;         // S: split-K parts per (token, head group); 1 for prefill
   int cols_per_split;   // raw columns per split
   int n_items;          // T * n_groups * n_splits
