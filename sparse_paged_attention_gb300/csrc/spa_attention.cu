@@ -410,8 +410,11 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         }
       }
       for (int j = 0; j < n_ti; ++j) {
-        // publish this tile to the MMA and softmax warps
-        mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+        // publish this tile to the MMA and softmax warps.  Only threads that write the entry
+        // wait for it to be free, and all of them have seen it free before it is published: a
+        // thread that waited without taking part could look only after the consumers had freed
+        // the entry's next use too, and then wait on a parity that never comes back.
+        if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
         if (kFp8) {
           const int idx = j * 128 + ptid;
           const int32_t code = idx < n ? list[idx] : -1;
@@ -493,14 +496,12 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       }
     }
     // end-of-work marker for the consumers
-    if (!*abort_flag) {
+    if (!*abort_flag && ptid == 0) {
       mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-      if (ptid == 0) {
-        ti[tik].item = -1;
-        ti[tik].n = 0;
-        ti[tik].flags = kFirst | kLast;
-        mbar_arrive(BAR(B_TIFULL + tik));
-      }
+      ti[tik].item = -1;
+      ti[tik].n = 0;
+      ti[tik].flags = kFirst | kLast;
+      mbar_arrive(BAR(B_TIFULL + tik));
     }
     cp_async_wait_all();
   } else if (warp == 4) {

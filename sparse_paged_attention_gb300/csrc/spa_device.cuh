@@ -209,7 +209,12 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// Named barrier over `count` threads (whole warps).  bar.sync is the warp-aligned form: a warp
+// must reach it converged, or it may be counted more than once and the barrier's later phases
+// pair up the wrong warps.  The warp is reconverged first, whatever divergent code (a lane-0
+// store, a per-lane poll loop) came before.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
