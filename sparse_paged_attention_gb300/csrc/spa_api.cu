@@ -101,6 +101,9 @@ void fill_pool(spa::PoolDev& d, const spa_pool_t* s) {
   d.bt = s->block_table;
   d.num_blocks = s->num_blocks;
   d.ps = s->page_size;
+  d.ps_shift = -1;
+  for (int k = 0; k < 31; ++k)
+    if (s->page_size == (1 << k)) d.ps_shift = k;
   d.bt_stride = s->bt_stride;
 }
 

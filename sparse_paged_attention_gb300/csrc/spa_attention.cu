@@ -52,18 +52,27 @@ struct TileInfo {                     // one entry of the tile-info ring
 constexpr int kRingOff = 0;
 constexpr int kQOff = kRingOff + kStages * kSlotBytes;      // 131072 (64 KB)
 constexpr int kPOff = kQOff + 65536;                        // 196608 (16 KB)
-constexpr int kListOff = kPOff + 16384;                     // 212992
-constexpr int kRedOff = kListOff + kMaxColumns * 4;         // 217088  float [2][4][64]
+constexpr int kListOff = kPOff + 16384;                     // 212992  int32 [2][kMaxColumns]
+constexpr int kRedOff = kListOff + 2 * kMaxColumns * 4;     // 221184  float [2][4][64]
 constexpr int kMrowOff = kRedOff + 2 * 4 * 64 * 4;          // 219136  float [4][64]
 constexpr int kArowOff = kMrowOff + 4 * 64 * 4;             // 220160  float [4][64]
 constexpr int kTiOff = kArowOff + 4 * 64 * 4;               // 221184  TileInfo [kTi]
 constexpr int kCntOff = kTiOff + kTi * (int)sizeof(TileInfo);
-constexpr int kBarOff = kCntOff + 64;
+constexpr int kInfoOff = kCntOff + 64;                      // ItemInfo [2]
+constexpr int kBarOff = kInfoOff + 32;
+
+struct ItemInfo {                     // one resolved item, handed from the resolver to the gather
+  int item;                           // -1: no more items
+  int n;                              // compacted columns in the item's list
+  float p_scale;                      // e4m3 only: 2^k applied to the probabilities
+  int pad;
+};
 
 enum {
   B_FULL = 0, B_EMPTY = 4, B_QFULL = 8, B_QEMPTY = 9, B_SFULL = 10, B_SEMPTY = 12,
   B_PFULL = 14, B_PVDONE = 15, B_OFREE = 16, B_TIFULL = 17, B_TIEMPTY = 21, B_RED = 25,
-  B_DRAIN = 27, B_READY = 28, B_RECV = 29, B_RECVML = 30, B_COUNT = 31
+  B_DRAIN = 27, B_READY = 28, B_RECV = 29, B_RECVML = 30, B_LFULL = 31, B_LEMPTY = 33,
+  B_COUNT = 35
 };
 constexpr int kMiscOff = kBarOff + B_COUNT * 8;             // TMEM base, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;            // + slack to align the base to 1 KB
@@ -206,8 +215,11 @@ __device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t lbo, uint32
   return d;
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+// kRes: a resolver warp (the tenth) walks the page tables of a CTA's next item while the gather
+// warps copy the current one; launched only when CTAs have more than one item.
+template <bool kFp8, bool kRes>
+__global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
+    attn_kernel(const __grid_constant__ AttnParams p) {
   using namespace cfg;
   using M = Mode<kFp8>;
   extern __shared__ uint8_t smem_raw[];
@@ -239,6 +251,10 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       mbar_init(BAR(B_TIEMPTY + i), 5);
     }
     mbar_init(BAR(B_DRAIN), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_LFULL + i), 1);    // the resolver's lane 0
+      mbar_init(BAR(B_LEMPTY + i), 4);   // lane 0 of every gather warp
+    }
     // cluster merge: one "ring idle" arrival from every CTA; the bulk copies of every CTA's
     // slice and (m, l) complete the receive barrier's transaction count, armed here
     mbar_init(BAR(B_READY), p.cluster > 1 ? p.cluster : 1);
@@ -271,11 +287,75 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
   const int n_mt = (D + 127) >> 7;        // 128-wide head_dim tiles of O^T
   const int C = p.rs.W + p.rs.K;
 
-  if (warp >= 5) {
+  if (kRes && warp == 9) {
+    // ==================================== resolve =====================================
+    // One warp walks the page tables of the next item while the gather warps copy the rows of
+    // the current one: two column lists, handed over through B_LFULL / B_LEMPTY.
+    // The CTA's first item is resolved by the gather warps themselves (nothing to overlap it
+    // with); this warp takes the u-th item, u >= 1, into list u & 1.
+    int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
+    ItemInfo* info = reinterpret_cast<ItemInfo*>(sm + kInfoOff);
+    for (int u = 1;; ++u) {
+      const long long item_ll = (long long)blockIdx.x + (long long)u * gridDim.x;
+      const int lb = u & 1;
+      if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
+      // the list is free once the gather warps are done with item u - 2
+      if (u >= 2 && !warp_wait(BAR(B_LEMPTY + lb), ((u - 2) >> 1) & 1, abort_flag)) break;
+      const int item = (int)item_ll;
+      const int s = item % p.n_splits;
+      const int tg = item / p.n_splits;
+      const int t = tg / p.n_groups;
+      const int c_lo = s * p.cols_per_split;
+      const int c_hi = min(C, c_lo + p.cols_per_split);
+      bool seq_ok;
+      const int b = seq_of(p.rs, t, &seq_ok);
+      const int pos = __ldg(p.rs.positions + t);
+      int32_t* list = lists + lb * kMaxColumns;
+      int n = 0;
+      float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
+      // 256 columns per round, eight per lane: the eight top-k reads, then the eight block-table
+      // reads, are each in flight together
+      for (int c0 = c_lo; c0 < c_hi; c0 += 256) {
+        ColumnPage cp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = c0 + k * 32 + lane;
+          cp[k] = (seq_ok && c < c_hi) ? column_page(p.rs, t, pos, c) : ColumnPage{-1, 0, 0};
+        }
+        int32_t code[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) code[k] = column_row(p.rs, b, cp[k]);
+        if (kFp8) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (code[k] >= 0) {
+              const float* vs = (code[k] >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
+              vmax = fmaxf(vmax, fabsf(__ldg(vs + (code[k] & ((1 << kColPoolShift) - 1)))));
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const unsigned m = __ballot_sync(0xffffffffu, code[k] >= 0);
+          if (code[k] >= 0) list[n + __popc(m & ((1u << lane) - 1u))] = code[k];
+          n += __popc(m);
+        }
+      }
+      float p_scale = 1.f;
+      if (kFp8 && n > 0) {
+        vmax = warp_max(vmax);
+        // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
+        p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
+      }
+      if (lane == 0) info[lb] = ItemInfo{item, n, p_scale, 0};
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_LFULL + lb));
+    }
+  } else if (warp >= 5) {
     // ===================================== gather ======================================
     const int ptid = threadIdx.x - 160;
     const int pw = warp - 5;
-    int32_t* list = reinterpret_cast<int32_t*>(sm + kListOff);
     volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);
     volatile float* fred = reinterpret_cast<volatile float*>(sm + kCntOff + 32);
     const int jj = ptid & 7, r0 = ptid >> 3;
@@ -284,60 +364,81 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
     const size_t row_bytes = (size_t)2 * D * M::kElt;  // K row then V row
     int ring = 0, tik = 0;
     uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-      // uniform abort check: one thread samples the flag, everyone reads the copy
+    int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
+    const ItemInfo* info = reinterpret_cast<const ItemInfo*>(sm + kInfoOff);
+    for (int u = 0;; ++u) {
+      const int lb = kRes ? (u & 1) : 0;
+      if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
+      // item u's column list: resolved right here for the first item (and for every item
+      // without a resolver warp), handed over by the resolver warp for the later ones
+      const bool handed = kRes && u > 0;
+      if (handed) mbar_wait(BAR(B_LFULL + lb), ((u - 1) >> 1) & 1, abort_flag);
+      // uniform abort check (one thread samples the flag, everyone reads the copy); it also
+      // catches a list wait that gave up
       named_bar_sync(2, 128);
       if (ptid == 0) cnt[4] = *abort_flag;
       named_bar_sync(2, 128);
       if (cnt[4]) break;
+      int item, n;
+      float p_scale = 1.f;
+      int32_t* list = lists + lb * kMaxColumns;
+      if (handed) {
+        const ItemInfo ii = info[lb];
+        item = ii.item;
+        n = ii.n;
+        p_scale = ii.p_scale;
+      } else {
+        item = (int)((long long)blockIdx.x + (long long)u * gridDim.x);
+        const int s0 = item % p.n_splits;
+        const int t0 = item / p.n_splits / p.n_groups;
+        const int c_lo = s0 * p.cols_per_split;
+        const int c_hi = min(C, c_lo + p.cols_per_split);
+        bool seq_ok;
+        const int b = seq_of(p.rs, t0, &seq_ok);
+        const int pos = __ldg(p.rs.positions + t0);
+        n = 0;
+        float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
+        for (int c0 = c_lo; c0 < c_hi; c0 += 128) {
+          const int c = c0 + ptid;
+          const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t0, b, pos, c) : -1;
+          if (kFp8 && code >= 0) {
+            const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
+            vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
+          if (lane == 0) cnt[pw] = __popc(m);
+          named_bar_sync(2, 128);
+          int off = n, tot = 0;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int cw = cnt[w];
+            off += (w < pw) ? cw : 0;
+            tot += cw;
+          }
+          if (code >= 0) list[off + __popc(m & ((1u << lane) - 1u))] = code;
+          n += tot;
+          named_bar_sync(2, 128);
+        }
+        if (kFp8 && n > 0) {
+          vmax = warp_max(vmax);
+          if (lane == 0) fred[pw] = vmax;
+          named_bar_sync(2, 128);
+          vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+          named_bar_sync(2, 128);
+          // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
+          p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
+        }
+      }
       const int s = item % p.n_splits;
       const int tg = item / p.n_splits;
       const int g = tg % p.n_groups;
       const int t = tg / p.n_groups;
-      const int c_lo = s * p.cols_per_split;
-      const int c_hi = min(C, c_lo + p.cols_per_split);
-      bool seq_ok;
-      const int b = seq_of(p.rs, t, &seq_ok);
-      const int pos = __ldg(p.rs.positions + t);
-      // resolve and compact the column set of this item
-      int n = 0;
-      float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
-      for (int c0 = c_lo; c0 < c_hi; c0 += 128) {
-        const int c = c0 + ptid;
-        const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t, b, pos, c) : -1;
-        if (kFp8 && code >= 0) {
-          const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
-          vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
-        if (lane == 0) cnt[pw] = __popc(m);
-        named_bar_sync(2, 128);
-        int off = n, tot = 0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int cw = cnt[w];
-          off += (w < pw) ? cw : 0;
-          tot += cw;
-        }
-        if (code >= 0) list[off + __popc(m & ((1u << lane) - 1u))] = code;
-        n += tot;
-        named_bar_sync(2, 128);
-      }
-      float q_scale = 1.f, p_scale = 1.f;
-      if (kFp8 && n > 0) {
-        vmax = warp_max(vmax);
-        if (lane == 0) fred[pw] = vmax;
-        named_bar_sync(2, 128);
-        vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
-        named_bar_sync(2, 128);
-        // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
-        p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
-      }
+      (void)s;
+      float q_scale = 1.f;
       const int n_tiles = (n + 127) >> 7;
-      const int n_ti = n_tiles > 0 ? n_tiles : 1;
       // Q of this token and head group.  Every item takes one turn of the buffer, also one
       // without columns.  The first item's bf16 q is loaded by the softmax warps at kernel
-      // start, in parallel with this walk of the page tables.
+      // start, while the resolver walks the first page tables.
       if (!kFp8 && item == (int)blockIdx.x) {
         q_ph ^= 1;
       } else {
@@ -409,90 +510,132 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
           mbar_arrive(BAR(B_QFULL));
         }
       }
-      for (int j = 0; j < n_ti; ++j) {
-        // publish this tile to the MMA and softmax warps.  Only threads that write the entry
-        // wait for it to be free, and all of them have seen it free before it is published: a
-        // thread that waited without taking part could look only after the consumers had freed
-        // the entry's next use too, and then wait on a parity that never comes back.
+      // Fill order of the ring: K0, K1, V0, K2, V1, ..., K(m-1), V(m-2), V(m-1): the MMA computes
+      // S(j+1) before PV(j), so the next tile's K is copied while the softmax works on this one.
+      // A single tile of at most 64 columns is packed: K in rows 0..63 and V in rows 64..127 of
+      // the same slots (the S MMA's rows past 63 are masked columns).
+      const bool packed = n_tiles == 1 && n <= 64;
+      const int n_steps = n == 0 ? 0 : (packed ? 1 : 2 * n_tiles);
+      const uint8_t* sc[8];   // rows of the newest tile whose K was copied
+      const uint8_t* sv[8];   // rows of the tile before it
+      int nj_c = 0, nj_v = 0;
+      if (n == 0) {
+        // no column: one tile-info entry tells the consumers
         if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
         if (kFp8) {
-          const int idx = j * 128 + ptid;
-          const int32_t code = idx < n ? list[idx] : -1;
-          float ks = 0.f, vs = 0.f;
-          if (code >= 0) {
-            const bool cmp = code >> kColPoolShift;
-            const int row = code & ((1 << kColPoolShift) - 1);
-            ks = __ldg((cmp ? p.rs.cmp.k_scale : p.rs.win.k_scale) + row);
-            vs = __ldg((cmp ? p.rs.cmp.v_scale : p.rs.win.v_scale) + row);
-          }
-          ti[tik].k_scale[ptid] = ks;
-          ti[tik].v_scale[ptid] = vs;
+          ti[tik].k_scale[ptid] = 0.f;
+          ti[tik].v_scale[ptid] = 0.f;
           named_bar_sync(2, 128);
         }
         if (ptid == 0) {
           TileInfo& e = ti[tik];
           e.item = item;
-          e.n = n == 0 ? 0 : min(128, n - j * 128);
-          e.flags = (j == 0 ? kFirst : 0) | (j == n_ti - 1 ? kLast : 0);
+          e.n = 0;
+          e.flags = kFirst | kLast;
           e.q_scale = q_scale;
           e.p_scale = p_scale;
           mbar_arrive(BAR(B_TIFULL + tik));
         }
         if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-        if (n == 0) break;
-        // the 8 rows of this tile that this thread copies
-        const uint8_t* src[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int idx = j * 128 + k * 16 + r0;
-          const int32_t code = idx < n ? list[idx] : -1;
-          if (code < 0) {
-            src[k] = nullptr;
-          } else {
-            const uint8_t* base = (code >> kColPoolShift) ? p.rs.cmp.kv : p.rs.win.kv;
-            src[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
+      }
+      for (int st = 0; st < n_steps; ++st) {
+        // step -> (tile, K or V)
+        int j, half;
+        if (st == 0) { j = 0; half = 0; }
+        else if (st == n_steps - 1) { j = n_tiles - 1; half = 1; }
+        else if (st & 1) { j = (st + 1) >> 1; half = 0; }
+        else { j = (st >> 1) - 1; half = 1; }
+        if (half == 0) {
+          // publish tile j to the MMA and softmax warps.  Only threads that write the entry
+          // wait for it to be free, and all of them have seen it free before it is published:
+          // a thread that waited without taking part could look only after the consumers had
+          // freed the entry's next use too, and then wait on a parity that never comes back.
+          if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+          if (kFp8) {
+            const int idx = j * 128 + ptid;
+            const int32_t code = idx < n ? list[idx] : -1;
+            float ks = 0.f, vs = 0.f;
+            if (code >= 0) {
+              const bool cmp = code >> kColPoolShift;
+              const int row = code & ((1 << kColPoolShift) - 1);
+              ks = __ldg((cmp ? p.rs.cmp.k_scale : p.rs.win.k_scale) + row);
+              vs = __ldg((cmp ? p.rs.cmp.v_scale : p.rs.win.v_scale) + row);
+            }
+            ti[tik].k_scale[ptid] = ks;
+            ti[tik].v_scale[ptid] = vs;
+            named_bar_sync(2, 128);
           }
+          if (ptid == 0) {
+            TileInfo& e = ti[tik];
+            e.item = item;
+            e.n = min(128, n - j * 128);
+            e.flags = (j == 0 ? kFirst : 0) | (j == n_tiles - 1 ? kLast : 0);
+            e.q_scale = q_scale;
+            e.p_scale = p_scale;
+            mbar_arrive(BAR(B_TIFULL + tik));
+          }
+          if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+          // the 8 rows of tile j that this thread copies
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            sv[k] = sc[k];
+            const int idx = j * 128 + k * 16 + r0;
+            const int32_t code = idx < n ? list[idx] : -1;
+            if (code < 0) {
+              sc[k] = nullptr;
+            } else {
+              const uint8_t* base = (code >> kColPoolShift) ? p.rs.cmp.kv : p.rs.win.kv;
+              sc[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
+            }
+          }
+          nj_v = nj_c;
+          nj_c = min(128, n - j * 128);
         }
+        // V of the newest tile only at the very last step; otherwise V of the tile before it
+        const bool cur = half == 0 || st == n_steps - 1;
+        const int nj = cur ? nj_c : nj_v;
         // Rows the MMAs read: the S MMA masks columns >= nj in the softmax, so K rows past nj
         // may hold anything; the PV MMA reads V rows up to its K-step multiple, which must be
         // zero past nj (zero probability times a stale NaN would still be NaN).  Row groups of
         // 16 past that bound are skipped with a warp-uniform test.
-        const int nj = min(128, n - j * 128);
         const int pv_step = kFp8 ? 32 : 16;
         const int v_rows = (nj + pv_step - 1) / pv_step * pv_step;
-        // A tile of at most 64 columns is packed: K in rows 0..63 and V in rows 64..127 of the
-        // same slots, so V lands with K (the S MMA's rows past 63 are masked columns).
-        const bool packed = nj <= 64;
+        const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
         const int kmax_v = packed ? (v_rows + 15) >> 4 : 0;
-        for (int half = 0; half < (packed ? 1 : 2); ++half) {  // K rows, then V rows
-          const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
-          for (int kc = 0; kc < n_chunks; ++kc) {
-            mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
-            const uint32_t d0 = sb + kRingOff + ring * kSlotBytes + dst_thread;
-            const bool a0 = (2 * kc) * 8 + jj < P16, a1 = (2 * kc + 1) * 8 + jj < P16;
-            const size_t so = (size_t)half * D * M::kElt + (size_t)(2 * kc) * 128 + jj * 16;
+        const uint8_t* sr[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if (k < kmax) {
-                const uint8_t* sp = src[k] ? src[k] + so : p.q;
-                const uint32_t sz = src[k] ? 16u : 0u;
-                if (a0) cp_async_16(d0 + k * 2048, sp, sz);
-                if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
-              }
-            }
+        for (int k = 0; k < 8; ++k) sr[k] = cur ? sc[k] : sv[k];
+        for (int kc = 0; kc < n_chunks; ++kc) {
+          mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
+          const uint32_t d0 = sb + kRingOff + ring * kSlotBytes + dst_thread;
+          const bool a0 = (2 * kc) * 8 + jj < P16, a1 = (2 * kc + 1) * 8 + jj < P16;
+          const size_t so = (size_t)half * D * M::kElt + (size_t)(2 * kc) * 128 + jj * 16;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              if (k < kmax_v) {
-                const uint8_t* sp = src[k] ? src[k] + so + D * M::kElt : p.q;
-                const uint32_t sz = src[k] ? 16u : 0u;
-                if (a0) cp_async_16(d0 + (4 + k) * 2048, sp, sz);
-                if (a1) cp_async_16(d0 + kAtomBytes + (4 + k) * 2048, sp + 128, sz);
-              }
+          for (int k = 0; k < 8; ++k) {
+            if (k < kmax) {
+              const uint8_t* sp = sr[k] ? sr[k] + so : p.q;
+              const uint32_t sz = sr[k] ? 16u : 0u;
+              if (a0) cp_async_16(d0 + k * 2048, sp, sz);
+              if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
             }
-            cp_async_arrive_noinc(BAR(B_FULL + ring));
-            if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
           }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (k < kmax_v) {
+              const uint8_t* sp = sr[k] ? sr[k] + so + D * M::kElt : p.q;
+              const uint32_t sz = sr[k] ? 16u : 0u;
+              if (a0) cp_async_16(d0 + (4 + k) * 2048, sp, sz);
+              if (a1) cp_async_16(d0 + kAtomBytes + (4 + k) * 2048, sp + 128, sz);
+            }
+          }
+          cp_async_arrive_noinc(BAR(B_FULL + ring));
+          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
         }
+      }
+      // this warp is done with the item's list
+      if (kRes) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_LEMPTY + lb));
       }
     }
     // end-of-work marker for the consumers
@@ -513,34 +656,16 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
       const uint32_t qbase = sb + kQOff, pbase = sb + kPOff;
       int ring = 0, tik = 0, sbuf = 0;
       uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
-      for (;;) {
-        if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
-        const int n = ti[tik].n;
-        const int item = ti[tik].item;
-        const int flags = ti[tik].flags;
-        mbar_arrive(BAR(B_TIEMPTY + tik));
-        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-        if (item < 0) break;
-        const bool first = flags & kFirst, last = flags & kLast;
-        if (first) {
-          if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;
-          q_ph ^= 1;
-        }
-        if (n == 0) {  // an item without columns: hand the Q buffer back untouched
-          mma_commit(BAR(B_QEMPTY));
-          continue;
-        }
-        if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) break;
+      // S of a tile: A = K rows from the ring (K-major), B = q (K-major), into S buffer sbuf.
+      // Releases the K slots unless the tile is packed (V still to be read from them).
+      auto issue_s = [&](bool packed) -> bool {
+        if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) return false;
         s_ph ^= 1u << sbuf;
         fence_proxy_async_smem();
         tc_fence_after();
-        bool ok = true;
         const uint32_t dS = tmem + sbuf * M::kSCols;
-        const bool packed = n <= 64;   // K and V share the slots (see the gather warps)
-        const int ring0 = ring;
-        const uint32_t ring_ph0 = ring_ph;
         for (int kc = 0; kc < n_chunks; ++kc) {
-          if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
+          if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
@@ -561,25 +686,23 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
           if (!packed) mma_commit(BAR(B_EMPTY + ring));
           if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
         }
-        if (!ok) break;
         mma_commit(BAR(B_SFULL + sbuf));
-        if (packed) {  // PV reads the same slots
-          ring = ring0;
-          ring_ph = ring_ph0;
-        }
-        const uint32_t v_off = packed ? 64u * 128u : 0u;
-        if (last) mma_commit(BAR(B_QEMPTY));
         sbuf ^= 1;
-        if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) break;
+        return true;
+      };
+      // PV of a tile of n columns: A = V^T from the ring (MN-major), B = P^T (MN-major).
+      auto issue_pv = [&](int n, bool first, bool packed) -> bool {
+        if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) return false;
         p_ph ^= 1;
         if (first) {
-          if (!mbar_wait(BAR(B_OFREE), o_ph ^ 1, abort_flag)) break;
+          if (!mbar_wait(BAR(B_OFREE), o_ph ^ 1, abort_flag)) return false;
           o_ph ^= 1;
         }
         fence_proxy_async_smem();
         tc_fence_after();
+        const uint32_t v_off = packed ? 64u * 128u : 0u;
         for (int vc = 0; vc < n_chunks; ++vc) {
-          if (!(ok = mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag))) break;
+          if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
@@ -612,8 +735,55 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
           mma_commit(BAR(B_EMPTY + ring));
           if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
         }
-        if (!ok) break;
         mma_commit(BAR(B_PVDONE));
+        return true;
+      };
+      // Per item: S(0); then for every tile j: S(j + 1) (if any), PV(j).  The tile-info entry of
+      // the next tile is read before PV of the current one.
+      bool ok = true;
+      for (;;) {
+        if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
+        int n = ti[tik].n;
+        const int item = ti[tik].item;
+        int flags = ti[tik].flags;
+        mbar_arrive(BAR(B_TIEMPTY + tik));
+        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+        if (item < 0) break;
+        if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;   // (every item begins a tile 0)
+        q_ph ^= 1;
+        if (n == 0) {  // an item without columns: hand the Q buffer back untouched
+          mma_commit(BAR(B_QEMPTY));
+          continue;
+        }
+        const bool packed = (flags & kLast) && n <= 64;   // a single packed tile
+        const int ring0 = ring;
+        const uint32_t ring_ph0 = ring_ph;
+        if (!(ok = issue_s(packed))) break;
+        if (flags & kLast) mma_commit(BAR(B_QEMPTY));
+        bool first = true;
+        for (;;) {
+          const bool last = flags & kLast;
+          int n_next = 0, flags_next = 0;
+          if (!last) {
+            if (!(ok = mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag))) break;
+            n_next = ti[tik].n;
+            flags_next = ti[tik].flags;
+            mbar_arrive(BAR(B_TIEMPTY + tik));
+            if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+            if (!(ok = issue_s(false))) break;
+            if (flags_next & kLast) mma_commit(BAR(B_QEMPTY));
+          }
+          if (packed) {  // PV reads the slots S just read
+            ring = ring0;
+            ring_ph = ring_ph0;
+          }
+          if (!(ok = issue_pv(n, first, packed))) break;
+          first = false;
+          if (last) break;
+          n = n_next;
+          flags = flags_next;
+        }
+        if (!ok) break;
       }
       // nothing may still write TMEM when it is released
       mma_commit(BAR(B_DRAIN));
@@ -725,8 +895,15 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         arow[lane] = a0;
         arow[32 + lane] = a1;
         __syncwarp();
+        if (!first) {
+          // wait for PV of the tile before (the MMA warp issues S of a tile before PV of the
+          // one before it): then O can be rescaled and the P buffer reused
+          if (!warp_wait(BAR(B_PVDONE), pv_ph, abort_flag)) break;
+          pv_ph ^= 1;
+          tc_fence_after();
+        }
         if (grow && !first) {
-          // the running max moved: rescale O (its last PV finished before this S was ready)
+          // the running max moved: rescale O
           for (int i = 0; i < n_mt; ++i) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -743,11 +920,6 @@ __global__ void __launch_bounds__(cfg::kThreads, 1) attn_kernel(const __grid_con
         }
         l0 *= a0;
         l1 *= a1;
-        if (!first) {
-          // P buffer reuse: the previous PV of this item is complete
-          if (!warp_wait(BAR(B_PVDONE), pv_ph, abort_flag)) break;
-          pv_ph ^= 1;
-        }
         // pass 2: probabilities, P^T row of this column, this warp's denominators
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -1139,10 +1311,20 @@ __global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ c
   cols[i] = ok ? resolve_column(a, t, b, __ldg(a.positions + t), c) : -1;
 }
 
+namespace {
+template <bool kFp8, bool kRes>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(attn_kernel<kFp8, kRes>);
+}
+const void* attn_kernel_ptr(bool fp8, bool res) {
+  if (fp8) return res ? kernel_ptr<true, true>() : kernel_ptr<true, false>();
+  return res ? kernel_ptr<false, true>() : kernel_ptr<false, false>();
+}
+}  // namespace
+
 cudaError_t prepare_attn_kernels() {
-  for (int f = 0; f < 2; ++f) {
-    const void* k = f ? reinterpret_cast<const void*>(attn_kernel<true>)
-                      : reinterpret_cast<const void*>(attn_kernel<false>);
+  for (int f = 0; f < 4; ++f) {
+    const void* k = attn_kernel_ptr(f & 1, f & 2);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1155,10 +1337,10 @@ cudaError_t prepare_attn_kernels() {
 
 namespace {
 cudaLaunchConfig_t attn_config(int grid, int cluster, cudaStream_t stream,
-                               cudaLaunchAttribute* attr) {
+                               cudaLaunchAttribute* attr, bool res) {
   cudaLaunchConfig_t c = {};
   c.gridDim = dim3((unsigned)grid, 1, 1);
-  c.blockDim = dim3(cfg::kThreads, 1, 1);
+  c.blockDim = dim3(res ? cfg::kThreads : cfg::kThreads - 32, 1, 1);
   c.dynamicSmemBytes = cfg::kSmemBytes;
   c.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1172,12 +1354,11 @@ cudaLaunchConfig_t attn_config(int grid, int cluster, cudaStream_t stream,
 }  // namespace
 
 int attn_max_active_clusters(int cluster, bool fp8) {
+  // cluster launches give every CTA one item: the kernel without the resolver warp
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c = attn_config(cluster, cluster, nullptr, attr);
+  cudaLaunchConfig_t c = attn_config(cluster, cluster, nullptr, attr, false);
   int n = 0;
-  const void* k = fp8 ? reinterpret_cast<const void*>(attn_kernel<true>)
-                      : reinterpret_cast<const void*>(attn_kernel<false>);
-  if (cudaOccupancyMaxActiveClusters(&n, k, &c) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel_ptr(fp8, false), &c) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1186,9 +1367,16 @@ int attn_max_active_clusters(int cluster, bool fp8) {
 
 cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr);
-  if (fp8) return cudaLaunchKernelEx(&c, attn_kernel<true>, p);
-  return cudaLaunchKernelEx(&c, attn_kernel<false>, p);
+  // a resolver warp pays off when CTAs have more than one item and the column sets are long
+  // enough that walking the page tables is a real share of an item (a single window tile is not)
+  const bool res = grid < p.n_items && p.rs.W + p.rs.K >= 256;
+  cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr, res);
+  if (fp8) {
+    if (res) return cudaLaunchKernelEx(&c, attn_kernel<true, true>, p);
+    return cudaLaunchKernelEx(&c, attn_kernel<true, false>, p);
+  }
+  if (res) return cudaLaunchKernelEx(&c, attn_kernel<false, true>, p);
+  return cudaLaunchKernelEx(&c, attn_kernel<false, false>, p);
 }
 
 int merge_max_splits() { return kMergeMaxSplits; }

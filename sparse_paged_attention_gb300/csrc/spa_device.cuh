@@ -19,6 +19,7 @@ struct PoolDev {
   const int32_t* bt;       // [num_seqs][bt_stride]
   long long num_blocks;
   int ps;
+  int ps_shift;            // log2(ps) when ps is a power of two, else -1
   int bt_stride;
 };
 
@@ -43,26 +44,68 @@ __device__ __forceinline__ void flag_error(int code) { atomicOr(&g_spa_error, co
 // Window column c < W holds token pos - W + 1 + c; top-k column holds entry topk[t][c - W],
 // present iff >= 0, r > 0 and r*j + r - 1 <= pos.  Out-of-table pages and out-of-pool blocks
 // are input errors: the column is dropped and SPA_ERR_INDEX is raised.
-__device__ __forceinline__ int32_t resolve_column(const ResolveArgs& a, int t, int b, int pos,
-                                                  int c) {
+//
+// Two steps, so that a caller resolving many columns can have all the loads of one step in
+// flight at once: column_page finds the pool, the page of the block table and the slot in the
+// page (it reads the top-k list), column_row reads the block table.
+struct ColumnPage {
+  int pool;   // 0 window, 1 compressed, -1 no column
+  int page;   // index into the sequence's block table (-1: beyond the table, an input error)
+  int slot;   // row within the page
+};
+
+// x = page * ps + slot for 0 <= x < 2^31 (a shift and a mask for the usual power-of-two pages)
+__device__ __forceinline__ void split_page(int x, const PoolDev& pl, int& page, int& slot) {
+  if (pl.ps_shift >= 0) {
+    page = x >> pl.ps_shift;
+    slot = x & (pl.ps - 1);
+  } else {
+    page = x / pl.ps;
+    slot = x - page * pl.ps;
+  }
+}
+
+__device__ __forceinline__ ColumnPage column_page(const ResolveArgs& a, int t, int pos, int c) {
+  ColumnPage cp{-1, 0, 0};
   if (c < a.W) {
     const long long x = (long long)pos - a.W + 1 + c;
-    if (x < 0) return -1;
-    const long long lp = x / a.win.ps;
-    if (lp >= a.win.bt_stride) { flag_error(SPA_ERR_INDEX); return -1; }
-    const int blk = __ldg(a.win.bt + (long long)b * a.win.bt_stride + lp);
-    if (blk < 0 || blk >= a.win.num_blocks) { flag_error(SPA_ERR_INDEX); return -1; }
-    return (int32_t)((long long)blk * a.win.ps + x % a.win.ps);
+    if (x < 0) return cp;
+    cp.pool = 0;
+    if (x <= 0x7fffffffLL) {
+      int lp;
+      split_page((int)x, a.win, lp, cp.slot);
+      cp.page = lp < a.win.bt_stride ? lp : -1;
+    } else {
+      const long long lp = x / a.win.ps;
+      cp.page = lp < a.win.bt_stride ? (int)lp : -1;
+      cp.slot = (int)(x % a.win.ps);
+    }
+    return cp;
   }
-  if (a.r <= 0) return -1;
+  if (a.r <= 0) return cp;
   const int j = __ldg(a.topk + (long long)t * a.K + (c - a.W));
-  if (j < 0) return -1;
-  if ((long long)a.r * j + a.r - 1 > pos) return -1;
-  const int lp = j / a.cmp.ps;
-  if (lp >= a.cmp.bt_stride) { flag_error(SPA_ERR_INDEX); return -1; }
-  const int blk = __ldg(a.cmp.bt + (long long)b * a.cmp.bt_stride + lp);
-  if (blk < 0 || blk >= a.cmp.num_blocks) { flag_error(SPA_ERR_INDEX); return -1; }
-  return (int32_t)((1u << kColPoolShift) | (uint32_t)((long long)blk * a.cmp.ps + j % a.cmp.ps));
+  if (j < 0) return cp;
+  if ((long long)a.r * j + a.r - 1 > pos) return cp;
+  int lp;
+  split_page(j, a.cmp, lp, cp.slot);
+  cp.pool = 1;
+  cp.page = lp < a.cmp.bt_stride ? lp : -1;
+  return cp;
+}
+
+__device__ __forceinline__ int32_t column_row(const ResolveArgs& a, int b, const ColumnPage& cp) {
+  if (cp.pool < 0) return -1;
+  const PoolDev& pl = cp.pool ? a.cmp : a.win;
+  if (cp.page < 0) { flag_error(SPA_ERR_INDEX); return -1; }
+  const int blk = __ldg(pl.bt + (long long)b * pl.bt_stride + cp.page);
+  if (blk < 0 || blk >= pl.num_blocks) { flag_error(SPA_ERR_INDEX); return -1; }
+  const uint32_t row = (uint32_t)((long long)blk * pl.ps + cp.slot);
+  return (int32_t)(cp.pool ? ((1u << kColPoolShift) | row) : row);
+}
+
+__device__ __forceinline__ int32_t resolve_column(const ResolveArgs& a, int t, int b, int pos,
+                                                  int c) {
+  return column_row(a, b, column_page(a, t, pos, c));
 }
 
 // Sequence of token t, checked against the table height.

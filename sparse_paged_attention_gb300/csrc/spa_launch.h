@@ -26,7 +26,7 @@ struct AttnParams {
 };
 
 // Kernel launch configuration.
-constexpr int kAttnThreads = 288;     // 4 softmax warps + 1 MMA warp + 4 gather warps
+constexpr int kAttnThreads = 320;     // 4 softmax, 1 MMA, 4 gather warps, 1 resolver warp
 int attn_smem_bytes();
 constexpr int kMaxColumns = 1024;     // window + top-k columns per query
 

@@ -131,6 +131,17 @@ def test_prefill_s8192_sampled():
     assert torch.equal(out[0].cpu(), v0.expand(d.w.num_heads, -1))
 
 
+def test_prefill_window_only_sampled():
+    """Window-only prefill over many queries per CTA (no resolver warp: each item's short column
+    set is resolved by the gather warps themselves)."""
+    d = OnDevice(make("prefill_s2048_r0"), _dev())
+    out = d.prefill()
+    check_no_device_error()
+    toks = _sample_tokens(d.w.num_tokens, 40, 2)
+    ref, _, _, _ = run_oracle(d.w, tokens=toks)
+    compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_BF16, what="prefill S2048 r0 (sampled)")
+
+
 # --- generality (FreeToken PR 633, "Correctness and tests": heads 20/16/128, windows 100/50,
 #     top-k widths that are not tile multiples, zero counts, the ratio-0 alias, pool views with a
 #     row offset) ---------------------------------------------------------------------------------
@@ -148,6 +159,8 @@ EDGE = {
     "row_offset": dict(num_heads=64, window=128, topk=100, ratio=4, head_dim=512, row_offset=3),
     "duplicates": dict(num_heads=8, window=8, topk=20, ratio=4, head_dim=64, duplicate_topk=True),
     "page1": dict(num_heads=8, window=20, topk=20, ratio=4, head_dim=64, page_size=1),
+    # a page size that is not a power of two takes the division path of the page lookup
+    "page24": dict(num_heads=8, window=40, topk=60, ratio=4, head_dim=64, page_size=24),
     "cols1024": dict(num_heads=64, window=512, topk=512, ratio=2, head_dim=512),
 }
 
