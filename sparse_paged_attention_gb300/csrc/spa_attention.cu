@@ -470,39 +470,51 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
               named_bar_sync(2, 128);
               q_scale = qm > 0.f ? pow2_floor(448.f / qm) : 1.f;
             }
-            for (int it = 0; it < 4 * n_atoms; ++it) {
-              const int h = (it & 3) * 16 + r0;
-              const int a = it >> 2;
-              const int piece = a * 8 + jj;      // 16 head_dim values
-              const int hg = g * p.gh + h;
-              const bool ok = h < p.gh && hg < p.H && piece < P16;
-              uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
-              if (ok) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    p.q + (((size_t)t * p.H + hg) * D + piece * 16) * 2);
-                u0 = __ldg(src);
-                u1 = __ldg(src + 1);
-              }
-              const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-              if (pass == 0) {
+            // four pieces per round, their eight 16-byte loads in flight together
+            for (int it0 = 0; it0 < 4 * n_atoms; it0 += 4) {
+              uint4 u[4][2];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                  qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
-              } else {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  uint32_t h0, l0, h1, l1;
-                  split_e4m3x2(bf16_lo(w[2 * k]) * q_scale, bf16_hi(w[2 * k]) * q_scale, h0, l0);
-                  split_e4m3x2(bf16_lo(w[2 * k + 1]) * q_scale, bf16_hi(w[2 * k + 1]) * q_scale, h1, l1);
-                  hi[k] = h0 | (h1 << 16);
-                  lo[k] = l0 | (l1 << 16);
+              for (int b4 = 0; b4 < 4; ++b4) {
+                const int it = it0 + b4;
+                const int h = (it & 3) * 16 + r0;
+                const int piece = (it >> 2) * 8 + jj;   // 16 head_dim values
+                const int hg = g * p.gh + h;
+                const bool ok = h < p.gh && hg < p.H && piece < P16;
+                u[b4][0] = u[b4][1] = make_uint4(0, 0, 0, 0);
+                if (ok) {
+                  const uint4* src = reinterpret_cast<const uint4*>(
+                      p.q + (((size_t)t * p.H + hg) * D + piece * 16) * 2);
+                  u[b4][0] = __ldg(src);
+                  u[b4][1] = __ldg(src + 1);
                 }
-                uint8_t* qrow = sm + kQOff + a * M::kQAtom;
-                *reinterpret_cast<uint4*>(qrow + h * 128 + ((jj ^ (h & 7)) << 4)) =
-                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(qrow + (64 + h) * 128 + ((jj ^ (h & 7)) << 4)) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              }
+#pragma unroll
+              for (int b4 = 0; b4 < 4; ++b4) {
+                const int it = it0 + b4;
+                const int h = (it & 3) * 16 + r0;
+                const int a = it >> 2;
+                const uint32_t w[8] = {u[b4][0].x, u[b4][0].y, u[b4][0].z, u[b4][0].w,
+                                       u[b4][1].x, u[b4][1].y, u[b4][1].z, u[b4][1].w};
+                if (pass == 0) {
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+                } else {
+                  uint32_t hi[4], lo[4];
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    uint32_t h0, l0, h1, l1;
+                    split_e4m3x2(bf16_lo(w[2 * k]) * q_scale, bf16_hi(w[2 * k]) * q_scale, h0, l0);
+                    split_e4m3x2(bf16_lo(w[2 * k + 1]) * q_scale, bf16_hi(w[2 * k + 1]) * q_scale, h1, l1);
+                    hi[k] = h0 | (h1 << 16);
+                    lo[k] = l0 | (l1 << 16);
+                  }
+                  uint8_t* qrow = sm + kQOff + a * M::kQAtom;
+                  *reinterpret_cast<uint4*>(qrow + h * 128 + ((jj ^ (h & 7)) << 4)) =
+                      make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                  *reinterpret_cast<uint4*>(qrow + (64 + h) * 128 + ((jj ^ (h & 7)) << 4)) =
+                      make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
               }
             }
           }
