@@ -175,6 +175,13 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Storage position of compacted column i in a column list.  Within each block of 128 columns,
+// column 16b + c is stored at 8c + b, so the eight columns a gather thread copies in one tile
+// (c fixed, b = 0..7) are eight consecutive words: two 16-byte loads.
+__device__ __forceinline__ int list_pos(int i) {
+  return (i & ~127) | ((i & 15) << 3) | ((i >> 4) & 7);
+}
+
 // 2^floor(log2 x) for finite x > 0 (clears the mantissa; x is kept within the normal range).
 __device__ __forceinline__ float pow2_floor(float x) {
   x = fminf(fmaxf(x, 1.17549435e-38f), 1.0e38f);
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const unsigned m = __ballot_sync(0xffffffffu, code[k] >= 0);
-          if (code[k] >= 0) list[n + __popc(m & ((1u << lane) - 1u))] = code[k];
+          if (code[k] >= 0) list[list_pos(n + __popc(m & ((1u << lane) - 1u)))] = code[k];
           n += __popc(m);
         }
       }
@@ -415,7 +422,7 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
             off += (w < pw) ? cw : 0;
             tot += cw;
           }
-          if (code >= 0) list[off + __popc(m & ((1u << lane) - 1u))] = code;
+          if (code >= 0) list[list_pos(off + __popc(m & ((1u << lane) - 1u)))] = code;
           n += tot;
           named_bar_sync(2, 128);
         }
@@ -565,7 +572,7 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
           if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
           if (kFp8) {
             const int idx = j * 128 + ptid;
-            const int32_t code = idx < n ? list[idx] : -1;
+            const int32_t code = idx < n ? list[list_pos(idx)] : -1;
             float ks = 0.f, vs = 0.f;
             if (code >= 0) {
               const bool cmp = code >> kColPoolShift;
@@ -587,12 +594,16 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
             mbar_arrive(BAR(B_TIFULL + tik));
           }
           if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-          // the 8 rows of tile j that this thread copies
+          // the 8 rows of tile j that this thread copies (columns j*128 + 16k + r0, stored
+          // consecutively)
+          const int4 lw0 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8);
+          const int4 lw1 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8 + 4);
+          const int32_t lc[8] = {lw0.x, lw0.y, lw0.z, lw0.w, lw1.x, lw1.y, lw1.z, lw1.w};
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             sv[k] = sc[k];
             const int idx = j * 128 + k * 16 + r0;
-            const int32_t code = idx < n ? list[idx] : -1;
+            const int32_t code = idx < n ? lc[k] : -1;
             if (code < 0) {
               sc[k] = nullptr;
             } else {
