@@ -72,6 +72,71 @@ int check_pool(const spa_pool_t* pl, bool fp8, int head_dim) {
 
 bool uses_cmp(const spa_problem_t* pr) { return pr->ratio > 0 && pr->topk > 0; }
 
+// ---- tensor maps of the bf16 pools (the kernel gathers their rows with tensor-map copies) ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return (EncodeTiledFn) nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// K rows (v = 0) or V rows (v = 1) of a pool [num_blocks][page_size][2][D] bf16 as a 2D byte
+// tensor: row i = token row i of the pool (2*D bytes), row stride 4*D bytes.  Boxes are 128 bytes
+// of one row; the 128-byte swizzle puts them straight into the MMA operand layout.
+bool encode_pool_rows(CUtensorMap* m, const spa_pool_t* pl, int D, int v) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  const cuuint64_t rows = (cuuint64_t)pl->num_blocks * (cuuint64_t)pl->page_size;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {2 * row_bytes};
+  const cuuint32_t box[2] = {128, 1};
+  const cuuint32_t elem[2] = {1, 1};
+  void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(pl->kv) + v * row_bytes);
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The maps of the last pools each host thread used, kept for the next call on the same pools.
+struct PoolMaps {
+  const void* kv = nullptr;
+  long long num_blocks = 0;
+  int page_size = 0, D = 0;
+  CUtensorMap map[2];
+};
+thread_local PoolMaps g_maps[2];
+
+bool pool_maps(CUtensorMap* out, const spa_pool_t* pl, int D, int which) {
+  PoolMaps& c = g_maps[which];
+  if (c.kv != pl->kv || c.num_blocks != pl->num_blocks || c.page_size != pl->page_size ||
+      c.D != D) {
+    c.kv = nullptr;
+    if (!encode_pool_rows(&c.map[0], pl, D, 0) || !encode_pool_rows(&c.map[1], pl, D, 1))
+      return false;
+    c.kv = pl->kv;
+    c.num_blocks = pl->num_blocks;
+    c.page_size = pl->page_size;
+    c.D = D;
+  }
+  out[0] = c.map[0];
+  out[1] = c.map[1];
+  return true;
+}
+
 int validate(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_problem_t* pr,
              const void* out, bool fp8) {
   if (!pr) return SPA_ERR_NULL;
@@ -251,6 +316,10 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   p.n_items = (int)items;
   // clustered: one item per CTA; otherwise a persistent grid of at most one CTA per SM
   const int grid = p.cluster > 1 ? (int)items : (int)(items < sms ? items : sms);
+  if (!fp8 && grid < items) {  // CTAs with several items gather bf16 rows by tensor maps
+    if (!pool_maps(&p.kv_map[0], win, pr->head_dim, 0)) return SPA_ERR_CUDA;
+    if (!pool_maps(&p.kv_map[2], uses_cmp(pr) ? cmp : win, pr->head_dim, 1)) return SPA_ERR_CUDA;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = spa::launch_attn(p, grid, fp8, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");

@@ -4,10 +4,11 @@
 // of the column list).  For each item it resolves and compacts the query's column set, then
 // streams it in tiles of 128 columns:
 //
-//   gather warps (5..8)  resolve columns through the block tables (FreeToken PR 633, "Changes":
-//                        per-column choice of window or compressed pool), then copy the 16-byte
-//                        pieces of every K and V row into shared memory with cp.async, already in
-//                        the 128-byte-swizzled operand layout, through a 4-slot ring.
+//   gather warps (5..)   resolve columns through the block tables (FreeToken PR 633, "Changes":
+//                        per-column choice of window or compressed pool), then copy every K and V
+//                        row into shared memory, already in the 128-byte-swizzled operand layout,
+//                        through a 4-slot ring: bf16 rows by tensor-map gathers (four rows of 128
+//                        bytes per copy, eight warps issuing), e4m3 rows by 16-byte cp.async.
 //   MMA warp (4)         S^T[c][h] = K[c][:] . Q[h][:]    tcgen05, M = 128 columns, N = heads
 //                        O^T[d][h] += V[c][d] * P^T[c][h] tcgen05, M = 128 of head_dim, N = 64
 //                        both accumulate in TMEM (S^T double-buffered, O^T resident).
@@ -35,7 +36,6 @@
 namespace spa {
 
 namespace cfg {
-constexpr int kThreads = kAttnThreads;
 constexpr int kStages = 4;            // K/V ring slots
 constexpr int kSlotBytes = 32768;     // 128 rows x 256 bytes (two 128-byte swizzle atoms)
 constexpr int kAtomBytes = 16384;     // 128 rows x 128 bytes
@@ -58,7 +58,7 @@ constexpr int kMrowOff = kRedOff + 2 * 4 * 64 * 4;          // 219136  float [4]
 constexpr int kArowOff = kMrowOff + 4 * 64 * 4;             // 220160  float [4][64]
 constexpr int kTiOff = kArowOff + 4 * 64 * 4;               // 221184  TileInfo [kTi]
 constexpr int kCntOff = kTiOff + kTi * (int)sizeof(TileInfo);
-constexpr int kInfoOff = kCntOff + 64;                      // ItemInfo [2]
+constexpr int kInfoOff = kCntOff + 128;                     // ItemInfo [2]
 constexpr int kBarOff = kInfoOff + 32;
 
 struct ItemInfo {                     // one resolved item, handed from the resolver to the gather
@@ -82,13 +82,16 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kFirst = 1, kLast = 2;
 }  // namespace cfg
 
-template <bool kFp8>
+template <bool kFp8, bool kTmaRows>
 struct Mode {
   static constexpr int kElt = kFp8 ? 1 : 2;        // bytes per K/V element
   static constexpr int kSCols = kFp8 ? 128 : 64;   // N of the S MMA (q, or q_hi | q_lo)
   static constexpr int kOCol = 2 * kSCols;         // first TMEM column of O^T
   static constexpr int kQAtom = kSCols * 128;      // bytes of one 128-byte-wide Q atom
   static constexpr float kTau = kFp8 ? 4.0f : 8.0f;  // lazy rescale threshold (log2 units)
+  static constexpr bool kTma = kTmaRows;           // rows by tensor-map gathers (else cp.async)
+  static constexpr int kNG = attn_gather_warps(kTmaRows);  // gather warps
+  static constexpr int kNGT = 32 * kNG;
 };
 
 int attn_smem_bytes() { return cfg::kSmemBytes; }
@@ -175,11 +178,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Storage position of compacted column i in a column list.  Within each block of 128 columns,
-// column 16b + c is stored at 8c + b, so the eight columns a gather thread copies in one tile
-// (c fixed, b = 0..7) are eight consecutive words: two 16-byte loads.
-__device__ __forceinline__ int list_pos(int i) {
-  return (i & ~127) | ((i & 15) << 3) | ((i >> 4) & 7);
+// Storage position of compacted column i in a column list.  Tensor-map gathers take four
+// consecutive columns, so their lists are in column order (natural).  For cp.async, within each
+// block of 128 columns, column 16b + c is stored at 8c + b, so the eight columns a gather thread
+// copies in one tile (c fixed, b = 0..7) are eight consecutive words: two 16-byte loads.
+__device__ __forceinline__ int list_pos(int i, bool natural) {
+  return natural ? i : ((i & ~127) | ((i & 15) << 3) | ((i >> 4) & 7));
 }
 
 // 2^floor(log2 x) for finite x > 0 (clears the mantissa; x is kept within the normal range).
@@ -222,13 +226,16 @@ __device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t lbo, uint32
   return d;
 }
 
-// kRes: a resolver warp (the tenth) walks the page tables of a CTA's next item while the gather
+// kRes: a resolver warp (the last) walks the page tables of a CTA's next item while the gather
 // warps copy the current one; launched only when CTAs have more than one item.
-template <bool kFp8, bool kRes>
-__global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
+// kTma: bf16 rows move by tensor-map gathers (CTAs with many items: throughput); otherwise by
+// cp.async, whose lower issue latency suits CTAs of a single item (decode) and e4m3 rows.
+template <bool kFp8, bool kRes, bool kTma>
+__global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
     attn_kernel(const __grid_constant__ AttnParams p) {
   using namespace cfg;
-  using M = Mode<kFp8>;
+  using M = Mode<kFp8, kTma>;
+  static_assert(!(kFp8 && kTma), "e4m3 rows are copied by cp.async");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -240,7 +247,9 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(BAR(B_FULL + i), 128);
+      // tensor maps: the armed arrivals of the pair of gather warps that fills the slot;
+      // cp.async: the noinc arrivals of the first 128 gather threads
+      mbar_init(BAR(B_FULL + i), M::kTma ? 2 : 128);
       mbar_init(BAR(B_EMPTY + i), 1);
     }
     mbar_init(BAR(B_QFULL), 128);
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
     mbar_init(BAR(B_DRAIN), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_LFULL + i), 1);    // the resolver's lane 0
-      mbar_init(BAR(B_LEMPTY + i), 4);   // lane 0 of every gather warp
+      mbar_init(BAR(B_LEMPTY + i), M::kNG);   // lane 0 of every gather warp
     }
     // cluster merge: one "ring idle" arrival from every CTA; the bulk copies of every CTA's
     // slice and (m, l) complete the receive barrier's transaction count, armed here
@@ -293,526 +302,609 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
   const int n_ks = P16 >> 1;              // 32-byte K steps of the S MMA
   const int n_mt = (D + 127) >> 7;        // 128-wide head_dim tiles of O^T
   const int C = p.rs.W + p.rs.K;
+  constexpr bool tma = M::kTma;
 
-  if (kRes && warp == 9) {
-    // ==================================== resolve =====================================
-    // One warp walks the page tables of the next item while the gather warps copy the rows of
-    // the current one: two column lists, handed over through B_LFULL / B_LEMPTY.
-    // The CTA's first item is resolved by the gather warps themselves (nothing to overlap it
-    // with); this warp takes the u-th item, u >= 1, into list u & 1.
-    int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
-    ItemInfo* info = reinterpret_cast<ItemInfo*>(sm + kInfoOff);
-    for (int u = 1;; ++u) {
-      const long long item_ll = (long long)blockIdx.x + (long long)u * gridDim.x;
-      const int lb = u & 1;
-      if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
-      // the list is free once the gather warps are done with item u - 2
-      if (u >= 2 && !warp_wait(BAR(B_LEMPTY + lb), ((u - 2) >> 1) & 1, abort_flag)) break;
-      const int item = (int)item_ll;
-      const int s = item % p.n_splits;
-      const int tg = item / p.n_splits;
-      const int t = tg / p.n_groups;
-      const int c_lo = s * p.cols_per_split;
-      const int c_hi = min(C, c_lo + p.cols_per_split);
-      bool seq_ok;
-      const int b = seq_of(p.rs, t, &seq_ok);
-      const int pos = __ldg(p.rs.positions + t);
-      int32_t* list = lists + lb * kMaxColumns;
-      int n = 0;
-      float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
-      // 256 columns per round, eight per lane: the eight top-k reads, then the eight block-table
-      // reads, are each in flight together
-      for (int c0 = c_lo; c0 < c_hi; c0 += 256) {
-        ColumnPage cp[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = c0 + k * 32 + lane;
-          cp[k] = (seq_ok && c < c_hi) ? column_page(p.rs, t, pos, c) : ColumnPage{-1, 0, 0};
-        }
-        int32_t code[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) code[k] = column_row(p.rs, b, cp[k]);
-        if (kFp8) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (code[k] >= 0) {
-              const float* vs = (code[k] >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
-              vmax = fmaxf(vmax, fabsf(__ldg(vs + (code[k] & ((1 << kColPoolShift) - 1)))));
-            }
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const unsigned m = __ballot_sync(0xffffffffu, code[k] >= 0);
-          if (code[k] >= 0) list[list_pos(n + __popc(m & ((1u << lane) - 1u)))] = code[k];
-          n += __popc(m);
-        }
-      }
-      float p_scale = 1.f;
-      if (kFp8 && n > 0) {
-        vmax = warp_max(vmax);
-        // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
-        p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
-      }
-      if (lane == 0) info[lb] = ItemInfo{item, n, p_scale, 0};
-      __threadfence_block();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_LFULL + lb));
-    }
-  } else if (warp >= 5) {
-    // ===================================== gather ======================================
-    const int ptid = threadIdx.x - 160;
-    const int pw = warp - 5;
-    volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);
-    volatile float* fred = reinterpret_cast<volatile float*>(sm + kCntOff + 32);
-    const int jj = ptid & 7, r0 = ptid >> 3;
-    // this thread copies chunk jj of rows r0, r0 + 16, ...: (r & 7) == (r0 & 7) for all of them
-    const uint32_t dst_thread = (uint32_t)(r0 * 128 + ((jj ^ (r0 & 7)) << 4));
-    const size_t row_bytes = (size_t)2 * D * M::kElt;  // K row then V row
-    int ring = 0, tik = 0;
-    uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
-    int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
-    const ItemInfo* info = reinterpret_cast<const ItemInfo*>(sm + kInfoOff);
-    for (int u = 0;; ++u) {
-      const int lb = kRes ? (u & 1) : 0;
-      if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
-      // item u's column list: resolved right here for the first item (and for every item
-      // without a resolver warp), handed over by the resolver warp for the later ones
-      const bool handed = kRes && u > 0;
-      if (handed) mbar_wait(BAR(B_LFULL + lb), ((u - 1) >> 1) & 1, abort_flag);
-      // uniform abort check (one thread samples the flag, everyone reads the copy); it also
-      // catches a list wait that gave up
-      named_bar_sync(2, 128);
-      if (ptid == 0) cnt[4] = *abort_flag;
-      named_bar_sync(2, 128);
-      if (cnt[4]) break;
-      int item, n;
-      float p_scale = 1.f;
-      int32_t* list = lists + lb * kMaxColumns;
-      if (handed) {
-        const ItemInfo ii = info[lb];
-        item = ii.item;
-        n = ii.n;
-        p_scale = ii.p_scale;
-      } else {
-        item = (int)((long long)blockIdx.x + (long long)u * gridDim.x);
-        const int s0 = item % p.n_splits;
-        const int t0 = item / p.n_splits / p.n_groups;
-        const int c_lo = s0 * p.cols_per_split;
+  if (warp >= 4) {
+    if (kRes && warp == 5 + M::kNG) {
+      // ==================================== resolve =====================================
+      // One warp walks the page tables of the next item while the gather warps copy the rows of
+      // the current one: two column lists, handed over through B_LFULL / B_LEMPTY.
+      // The CTA's first item is resolved by the gather warps themselves (nothing to overlap it
+      // with); this warp takes the u-th item, u >= 1, into list u & 1.
+      int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
+      ItemInfo* info = reinterpret_cast<ItemInfo*>(sm + kInfoOff);
+      for (int u = 1;; ++u) {
+        const long long item_ll = (long long)blockIdx.x + (long long)u * gridDim.x;
+        const int lb = u & 1;
+        if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
+        // the list is free once the gather warps are done with item u - 2
+        if (u >= 2 && !warp_wait(BAR(B_LEMPTY + lb), ((u - 2) >> 1) & 1, abort_flag)) break;
+        const int item = (int)item_ll;
+        const int s = item % p.n_splits;
+        const int tg = item / p.n_splits;
+        const int t = tg / p.n_groups;
+        const int c_lo = s * p.cols_per_split;
         const int c_hi = min(C, c_lo + p.cols_per_split);
         bool seq_ok;
-        const int b = seq_of(p.rs, t0, &seq_ok);
-        const int pos = __ldg(p.rs.positions + t0);
-        n = 0;
+        const int b = seq_of(p.rs, t, &seq_ok);
+        const int pos = __ldg(p.rs.positions + t);
+        int32_t* list = lists + lb * kMaxColumns;
+        int n = 0;
         float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
-        for (int c0 = c_lo; c0 < c_hi; c0 += 128) {
-          const int c = c0 + ptid;
-          const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t0, b, pos, c) : -1;
-          if (kFp8 && code >= 0) {
-            const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
-            vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));
-          }
-          const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
-          if (lane == 0) cnt[pw] = __popc(m);
-          named_bar_sync(2, 128);
-          int off = n, tot = 0;
+        // 256 columns per round, eight per lane: the eight top-k reads, then the eight block-table
+        // reads, are each in flight together
+        for (int c0 = c_lo; c0 < c_hi; c0 += 256) {
+          ColumnPage cp[8];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int cw = cnt[w];
-            off += (w < pw) ? cw : 0;
-            tot += cw;
+          for (int k = 0; k < 8; ++k) {
+            const int c = c0 + k * 32 + lane;
+            cp[k] = (seq_ok && c < c_hi) ? column_page(p.rs, t, pos, c) : ColumnPage{-1, 0, 0};
           }
-          if (code >= 0) list[list_pos(off + __popc(m & ((1u << lane) - 1u)))] = code;
-          n += tot;
-          named_bar_sync(2, 128);
+          int32_t code[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) code[k] = column_row(p.rs, b, cp[k]);
+          if (kFp8) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (code[k] >= 0) {
+                const float* vs = (code[k] >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
+                vmax = fmaxf(vmax, fabsf(__ldg(vs + (code[k] & ((1 << kColPoolShift) - 1)))));
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const unsigned m = __ballot_sync(0xffffffffu, code[k] >= 0);
+            if (code[k] >= 0) list[list_pos(n + __popc(m & ((1u << lane) - 1u)), tma)] = code[k];
+            n += __popc(m);
+          }
         }
+        float p_scale = 1.f;
         if (kFp8 && n > 0) {
           vmax = warp_max(vmax);
-          if (lane == 0) fred[pw] = vmax;
-          named_bar_sync(2, 128);
-          vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
-          named_bar_sync(2, 128);
           // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
           p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
         }
+        if (lane == 0) info[lb] = ItemInfo{item, n, p_scale, 0};
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_LFULL + lb));
       }
-      const int s = item % p.n_splits;
-      const int tg = item / p.n_splits;
-      const int g = tg % p.n_groups;
-      const int t = tg / p.n_groups;
-      (void)s;
-      float q_scale = 1.f;
-      const int n_tiles = (n + 127) >> 7;
-      // Q of this token and head group.  Every item takes one turn of the buffer, also one
-      // without columns.  The first item's bf16 q is loaded by the softmax warps at kernel
-      // start, while the resolver walks the first page tables.
-      if (!kFp8 && item == (int)blockIdx.x) {
-        q_ph ^= 1;
-      } else {
-        mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
-        q_ph ^= 1;
-        if (n == 0) {
-          mbar_arrive(BAR(B_QFULL));
-        } else if (!kFp8) {
-          const uint32_t qs = sb + kQOff;
-          // bf16: [atom][64 heads][128 B], heads beyond H zero-filled
-          for (int it = 0; it < 4 * n_atoms; ++it) {
-            const int h = (it & 3) * 16 + r0;
-            const int a = it >> 2;
-            const int hg = g * p.gh + h;
-            const bool ok = h < p.gh && hg < p.H;
-            const uint8_t* src = p.q + (((size_t)t * p.H + (ok ? hg : 0)) * D) * 2 + a * 128 + jj * 16;
-            cp_async_16(qs + a * M::kQAtom + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(BAR(B_QFULL));
+    } else if (warp >= 5 && warp < 5 + M::kNG) {
+      // ===================================== gather ======================================
+      constexpr int NG = M::kNG, NGT = M::kNGT;
+      static_assert(!kFp8 || NG == 4, "the e4m3 path's per-column work assumes 128 gather threads");
+      static_assert(!M::kTma || NG % 2 == 0, "tensor-map gathers run in pairs of warps");
+      const int ptid = threadIdx.x - 160;
+      const int pw = warp - 5;
+      volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);            // [16]
+      volatile int* abort_copy = cnt + 16;
+      volatile float* fred = reinterpret_cast<volatile float*>(sm + kCntOff + 80);  // [8]
+      const int jj = ptid & 7, r0 = ptid >> 3;
+      // cp.async: this thread copies chunk jj of rows r0, r0 + 16, ...: (r & 7) == (r0 & 7) for all
+      const uint32_t dst_thread = (uint32_t)(r0 * 128 + ((jj ^ (r0 & 7)) << 4));
+      const size_t row_bytes = (size_t)2 * D * M::kElt;  // K row then V row
+      int ring = 0, tik = 0;
+      uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
+      int fills = 0;  // ring slots this thread has filled
+      int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
+      const ItemInfo* info = reinterpret_cast<const ItemInfo*>(sm + kInfoOff);
+      for (int u = 0;; ++u) {
+        const int lb = kRes ? (u & 1) : 0;
+        if ((long long)blockIdx.x + (long long)u * gridDim.x >= p.n_items) break;
+        // item u's column list: resolved right here for the first item (and for every item
+        // without a resolver warp), handed over by the resolver warp for the later ones
+        const bool handed = kRes && u > 0;
+        if (handed) mbar_wait(BAR(B_LFULL + lb), ((u - 1) >> 1) & 1, abort_flag);
+        // uniform abort check (one thread samples the flag, everyone reads the copy); it also
+        // catches a list wait that gave up
+        named_bar_sync(2, NGT);
+        if (ptid == 0) *abort_copy = *abort_flag;
+        named_bar_sync(2, NGT);
+        if (*abort_copy) break;
+        int item, n;
+        float p_scale = 1.f;
+        int32_t* list = lists + lb * kMaxColumns;
+        if (handed) {
+          const ItemInfo ii = info[lb];
+          item = ii.item;
+          n = ii.n;
+          p_scale = ii.p_scale;
         } else {
-          // e4m3: rows 0..63 hold q_hi, rows 64..127 q_lo, both times a power of two per token
-          float qm = 0.f;
-          for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 1) {
-              qm = warp_max(qm);
-              if (lane == 0) fred[pw] = qm;
-              named_bar_sync(2, 128);
-              qm = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
-              named_bar_sync(2, 128);
-              q_scale = qm > 0.f ? pow2_floor(448.f / qm) : 1.f;
+          item = (int)((long long)blockIdx.x + (long long)u * gridDim.x);
+          const int s0 = item % p.n_splits;
+          const int t0 = item / p.n_splits / p.n_groups;
+          const int c_lo = s0 * p.cols_per_split;
+          const int c_hi = min(C, c_lo + p.cols_per_split);
+          bool seq_ok;
+          const int b = seq_of(p.rs, t0, &seq_ok);
+          const int pos = __ldg(p.rs.positions + t0);
+          n = 0;
+          float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
+          for (int c0 = c_lo; c0 < c_hi; c0 += NGT) {
+            const int c = c0 + ptid;
+            const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t0, b, pos, c) : -1;
+            if (kFp8 && code >= 0) {
+              const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
+              vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));
             }
-            // four pieces per round, their eight 16-byte loads in flight together
-            for (int it0 = 0; it0 < 4 * n_atoms; it0 += 4) {
-              uint4 u[4][2];
+            const unsigned m = __ballot_sync(0xffffffffu, code >= 0);
+            if (lane == 0) cnt[pw] = __popc(m);
+            named_bar_sync(2, NGT);
+            int off = n, tot = 0;
 #pragma unroll
-              for (int b4 = 0; b4 < 4; ++b4) {
-                const int it = it0 + b4;
-                const int h = (it & 3) * 16 + r0;
-                const int piece = (it >> 2) * 8 + jj;   // 16 head_dim values
-                const int hg = g * p.gh + h;
-                const bool ok = h < p.gh && hg < p.H && piece < P16;
-                u[b4][0] = u[b4][1] = make_uint4(0, 0, 0, 0);
-                if (ok) {
-                  const uint4* src = reinterpret_cast<const uint4*>(
-                      p.q + (((size_t)t * p.H + hg) * D + piece * 16) * 2);
-                  u[b4][0] = __ldg(src);
-                  u[b4][1] = __ldg(src + 1);
-                }
-              }
-#pragma unroll
-              for (int b4 = 0; b4 < 4; ++b4) {
-                const int it = it0 + b4;
-                const int h = (it & 3) * 16 + r0;
-                const int a = it >> 2;
-                const uint32_t w[8] = {u[b4][0].x, u[b4][0].y, u[b4][0].z, u[b4][0].w,
-                                       u[b4][1].x, u[b4][1].y, u[b4][1].z, u[b4][1].w};
-                if (pass == 0) {
-#pragma unroll
-                  for (int k = 0; k < 8; ++k)
-                    qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
-                } else {
-                  uint32_t hi[4], lo[4];
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    uint32_t h0, l0, h1, l1;
-                    split_e4m3x2(bf16_lo(w[2 * k]) * q_scale, bf16_hi(w[2 * k]) * q_scale, h0, l0);
-                    split_e4m3x2(bf16_lo(w[2 * k + 1]) * q_scale, bf16_hi(w[2 * k + 1]) * q_scale, h1, l1);
-                    hi[k] = h0 | (h1 << 16);
-                    lo[k] = l0 | (l1 << 16);
-                  }
-                  uint8_t* qrow = sm + kQOff + a * M::kQAtom;
-                  *reinterpret_cast<uint4*>(qrow + h * 128 + ((jj ^ (h & 7)) << 4)) =
-                      make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                  *reinterpret_cast<uint4*>(qrow + (64 + h) * 128 + ((jj ^ (h & 7)) << 4)) =
-                      make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-              }
+            for (int w = 0; w < NG; ++w) {
+              const int cw = cnt[w];
+              off += (w < pw) ? cw : 0;
+              tot += cw;
             }
+            if (code >= 0) list[list_pos(off + __popc(m & ((1u << lane) - 1u)), tma)] = code;
+            n += tot;
+            named_bar_sync(2, NGT);
           }
-          fence_proxy_async_smem();
-          mbar_arrive(BAR(B_QFULL));
+          if (kFp8 && n > 0) {
+            vmax = warp_max(vmax);
+            if (lane == 0) fred[pw] = vmax;
+            named_bar_sync(2, NGT);
+            vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+            named_bar_sync(2, NGT);
+            // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
+            p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
+          }
         }
-      }
-      // Fill order of the ring: K0, K1, V0, K2, V1, ..., K(m-1), V(m-2), V(m-1): the MMA computes
-      // S(j+1) before PV(j), so the next tile's K is copied while the softmax works on this one.
-      // A single tile of at most 64 columns is packed: K in rows 0..63 and V in rows 64..127 of
-      // the same slots (the S MMA's rows past 63 are masked columns).
-      const bool packed = n_tiles == 1 && n <= 64;
-      const int n_steps = n == 0 ? 0 : (packed ? 1 : 2 * n_tiles);
-      const uint8_t* sc[8];   // rows of the newest tile whose K was copied
-      const uint8_t* sv[8];   // rows of the tile before it
-      int nj_c = 0, nj_v = 0;
-      if (n == 0) {
-        // no column: one tile-info entry tells the consumers
-        if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-        if (kFp8) {
-          ti[tik].k_scale[ptid] = 0.f;
-          ti[tik].v_scale[ptid] = 0.f;
-          named_bar_sync(2, 128);
+        const int s = item % p.n_splits;
+        const int tg = item / p.n_splits;
+        const int g = tg % p.n_groups;
+        const int t = tg / p.n_groups;
+        (void)s;
+        float q_scale = 1.f;
+        const int n_tiles = (n + 127) >> 7;
+        // Q of this token and head group, loaded by the first 128 gather threads.  Every item takes
+        // one turn of the buffer, also one without columns.  The first item's bf16 q is loaded by
+        // the softmax warps at kernel start, while the resolver walks the first page tables.
+        if (!kFp8 && item == (int)blockIdx.x) {
+          q_ph ^= 1;
+        } else if (ptid < 128) {
+          mbar_wait(BAR(B_QEMPTY), q_ph ^ 1, abort_flag);
+          q_ph ^= 1;
+          if (n == 0) {
+            mbar_arrive(BAR(B_QFULL));
+          } else if (!kFp8) {
+            const uint32_t qs = sb + kQOff;
+            // bf16: [atom][64 heads][128 B], heads beyond H zero-filled
+            for (int it = 0; it < 4 * n_atoms; ++it) {
+              const int h = (it & 3) * 16 + r0;
+              const int a = it >> 2;
+              const int hg = g * p.gh + h;
+              const bool ok = h < p.gh && hg < p.H;
+              const uint8_t* src = p.q + (((size_t)t * p.H + (ok ? hg : 0)) * D) * 2 + a * 128 + jj * 16;
+              cp_async_16(qs + a * M::kQAtom + h * 128 + ((jj ^ (h & 7)) << 4), src, ok ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(BAR(B_QFULL));
+          } else {
+            // e4m3: rows 0..63 hold q_hi, rows 64..127 q_lo, both times a power of two per token
+            float qm = 0.f;
+            for (int pass = 0; pass < 2; ++pass) {
+              if (pass == 1) {
+                qm = warp_max(qm);
+                if (lane == 0) fred[pw] = qm;
+                named_bar_sync(2, 128);
+                qm = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+                named_bar_sync(2, 128);
+                q_scale = qm > 0.f ? pow2_floor(448.f / qm) : 1.f;
+              }
+              // four pieces per round, their eight 16-byte loads in flight together
+              for (int it0 = 0; it0 < 4 * n_atoms; it0 += 4) {
+                uint4 u[4][2];
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) {
+                  const int it = it0 + b4;
+                  const int h = (it & 3) * 16 + r0;
+                  const int piece = (it >> 2) * 8 + jj;   // 16 head_dim values
+                  const int hg = g * p.gh + h;
+                  const bool ok = h < p.gh && hg < p.H && piece < P16;
+                  u[b4][0] = u[b4][1] = make_uint4(0, 0, 0, 0);
+                  if (ok) {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        p.q + (((size_t)t * p.H + hg) * D + piece * 16) * 2);
+                    u[b4][0] = __ldg(src);
+                    u[b4][1] = __ldg(src + 1);
+                  }
+                }
+#pragma unroll
+                for (int b4 = 0; b4 < 4; ++b4) {
+                  const int it = it0 + b4;
+                  const int h = (it & 3) * 16 + r0;
+                  const int a = it >> 2;
+                  const uint32_t w[8] = {u[b4][0].x, u[b4][0].y, u[b4][0].z, u[b4][0].w,
+                                         u[b4][1].x, u[b4][1].y, u[b4][1].z, u[b4][1].w};
+                  if (pass == 0) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                      qm = fmaxf(qm, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+                  } else {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                      uint32_t h0, l0, h1, l1;
+                      split_e4m3x2(bf16_lo(w[2 * k]) * q_scale, bf16_hi(w[2 * k]) * q_scale, h0, l0);
+                      split_e4m3x2(bf16_lo(w[2 * k + 1]) * q_scale, bf16_hi(w[2 * k + 1]) * q_scale, h1, l1);
+                      hi[k] = h0 | (h1 << 16);
+                      lo[k] = l0 | (l1 << 16);
+                    }
+                    uint8_t* qrow = sm + kQOff + a * M::kQAtom;
+                    *reinterpret_cast<uint4*>(qrow + h * 128 + ((jj ^ (h & 7)) << 4)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(qrow + (64 + h) * 128 + ((jj ^ (h & 7)) << 4)) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                  }
+                }
+              }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(BAR(B_QFULL));
+          }
         }
-        if (ptid == 0) {
-          TileInfo& e = ti[tik];
-          e.item = item;
-          e.n = 0;
-          e.flags = kFirst | kLast;
-          e.q_scale = q_scale;
-          e.p_scale = p_scale;
-          mbar_arrive(BAR(B_TIFULL + tik));
-        }
-        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-      }
-      for (int st = 0; st < n_steps; ++st) {
-        // step -> (tile, K or V)
-        int j, half;
-        if (st == 0) { j = 0; half = 0; }
-        else if (st == n_steps - 1) { j = n_tiles - 1; half = 1; }
-        else if (st & 1) { j = (st + 1) >> 1; half = 0; }
-        else { j = (st >> 1) - 1; half = 1; }
-        if (half == 0) {
-          // publish tile j to the MMA and softmax warps.  Only threads that write the entry
-          // wait for it to be free, and all of them have seen it free before it is published:
-          // a thread that waited without taking part could look only after the consumers had
-          // freed the entry's next use too, and then wait on a parity that never comes back.
+        // Fill order of the ring: K0, K1, V0, K2, V1, ..., K(m-1), V(m-2), V(m-1): the MMA computes
+        // S(j+1) before PV(j), so the next tile's K is copied while the softmax works on this one.
+        // A single tile of at most 64 columns is packed: K in rows 0..63 and V in rows 64..127 of
+        // the same slots (the S MMA's rows past 63 are masked columns).
+        const bool packed = n_tiles == 1 && n <= 64;
+        const int n_steps = n == 0 ? 0 : (packed ? 1 : 2 * n_tiles);
+        const uint8_t* sc[8];   // rows of the newest tile whose K was copied
+        const uint8_t* sv[8];   // rows of the tile before it
+        int nj_c = 0, nj_v = 0;
+        if (n == 0) {
+          // no column: one tile-info entry tells the consumers
           if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
           if (kFp8) {
-            const int idx = j * 128 + ptid;
-            const int32_t code = idx < n ? list[list_pos(idx)] : -1;
-            float ks = 0.f, vs = 0.f;
-            if (code >= 0) {
-              const bool cmp = code >> kColPoolShift;
-              const int row = code & ((1 << kColPoolShift) - 1);
-              ks = __ldg((cmp ? p.rs.cmp.k_scale : p.rs.win.k_scale) + row);
-              vs = __ldg((cmp ? p.rs.cmp.v_scale : p.rs.win.v_scale) + row);
-            }
-            ti[tik].k_scale[ptid] = ks;
-            ti[tik].v_scale[ptid] = vs;
+            ti[tik].k_scale[ptid] = 0.f;
+            ti[tik].v_scale[ptid] = 0.f;
             named_bar_sync(2, 128);
           }
           if (ptid == 0) {
             TileInfo& e = ti[tik];
             e.item = item;
-            e.n = min(128, n - j * 128);
-            e.flags = (j == 0 ? kFirst : 0) | (j == n_tiles - 1 ? kLast : 0);
+            e.n = 0;
+            e.flags = kFirst | kLast;
             e.q_scale = q_scale;
             e.p_scale = p_scale;
             mbar_arrive(BAR(B_TIFULL + tik));
           }
           if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-          // the 8 rows of tile j that this thread copies (columns j*128 + 16k + r0, stored
-          // consecutively)
-          const int4 lw0 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8);
-          const int4 lw1 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8 + 4);
-          const int32_t lc[8] = {lw0.x, lw0.y, lw0.z, lw0.w, lw1.x, lw1.y, lw1.z, lw1.w};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            sv[k] = sc[k];
-            const int idx = j * 128 + k * 16 + r0;
-            const int32_t code = idx < n ? lc[k] : -1;
-            if (code < 0) {
-              sc[k] = nullptr;
-            } else {
-              const uint8_t* base = (code >> kColPoolShift) ? p.rs.cmp.kv : p.rs.win.kv;
-              sc[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
-            }
-          }
-          nj_v = nj_c;
-          nj_c = min(128, n - j * 128);
         }
-        // V of the newest tile only at the very last step; otherwise V of the tile before it
-        const bool cur = half == 0 || st == n_steps - 1;
-        const int nj = cur ? nj_c : nj_v;
-        // Rows the MMAs read: the S MMA masks columns >= nj in the softmax, so K rows past nj
-        // may hold anything; the PV MMA reads V rows up to its K-step multiple, which must be
-        // zero past nj (zero probability times a stale NaN would still be NaN).  Row groups of
-        // 16 past that bound are skipped with a warp-uniform test.
-        const int pv_step = kFp8 ? 32 : 16;
-        const int v_rows = (nj + pv_step - 1) / pv_step * pv_step;
-        const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
-        const int kmax_v = packed ? (v_rows + 15) >> 4 : 0;
-        const uint8_t* sr[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sr[k] = cur ? sc[k] : sv[k];
-        for (int kc = 0; kc < n_chunks; ++kc) {
-          mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
-          const uint32_t d0 = sb + kRingOff + ring * kSlotBytes + dst_thread;
-          const bool a0 = (2 * kc) * 8 + jj < P16, a1 = (2 * kc + 1) * 8 + jj < P16;
-          const size_t so = (size_t)half * D * M::kElt + (size_t)(2 * kc) * 128 + jj * 16;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (k < kmax) {
-              const uint8_t* sp = sr[k] ? sr[k] + so : p.q;
-              const uint32_t sz = sr[k] ? 16u : 0u;
-              if (a0) cp_async_16(d0 + k * 2048, sp, sz);
-              if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
+        for (int st = 0; st < n_steps; ++st) {
+          // step -> (tile, K or V)
+          int j, half;
+          if (st == 0) { j = 0; half = 0; }
+          else if (st == n_steps - 1) { j = n_tiles - 1; half = 1; }
+          else if (st & 1) { j = (st + 1) >> 1; half = 0; }
+          else { j = (st >> 1) - 1; half = 1; }
+          if (half == 0) {
+            // publish tile j to the MMA and softmax warps.  Only threads that write the entry
+            // wait for it to be free, and all of them have seen it free before it is published:
+            // a thread that waited without taking part could look only after the consumers had
+            // freed the entry's next use too, and then wait on a parity that never comes back.
+            if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+            if (kFp8) {
+              const int idx = j * 128 + ptid;
+              const int32_t code = idx < n ? list[list_pos(idx, tma)] : -1;
+              float ks = 0.f, vs = 0.f;
+              if (code >= 0) {
+                const bool cmp = code >> kColPoolShift;
+                const int row = code & ((1 << kColPoolShift) - 1);
+                ks = __ldg((cmp ? p.rs.cmp.k_scale : p.rs.win.k_scale) + row);
+                vs = __ldg((cmp ? p.rs.cmp.v_scale : p.rs.win.v_scale) + row);
+              }
+              ti[tik].k_scale[ptid] = ks;
+              ti[tik].v_scale[ptid] = vs;
+              named_bar_sync(2, 128);
             }
-          }
+            if (ptid == 0) {
+              TileInfo& e = ti[tik];
+              e.item = item;
+              e.n = min(128, n - j * 128);
+              e.flags = (j == 0 ? kFirst : 0) | (j == n_tiles - 1 ? kLast : 0);
+              e.q_scale = q_scale;
+              e.p_scale = p_scale;
+              mbar_arrive(BAR(B_TIFULL + tik));
+            }
+            if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+            if (!tma && ptid < 128) {
+              // the 8 rows of tile j that this thread copies (columns j*128 + 16k + r0, stored
+              // consecutively)
+              const int4 lw0 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8);
+              const int4 lw1 = *reinterpret_cast<const int4*>(list + j * 128 + r0 * 8 + 4);
+              const int32_t lc[8] = {lw0.x, lw0.y, lw0.z, lw0.w, lw1.x, lw1.y, lw1.z, lw1.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if (k < kmax_v) {
-              const uint8_t* sp = sr[k] ? sr[k] + so + D * M::kElt : p.q;
-              const uint32_t sz = sr[k] ? 16u : 0u;
-              if (a0) cp_async_16(d0 + (4 + k) * 2048, sp, sz);
-              if (a1) cp_async_16(d0 + kAtomBytes + (4 + k) * 2048, sp + 128, sz);
-            }
-          }
-          cp_async_arrive_noinc(BAR(B_FULL + ring));
-          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
-        }
-      }
-      // this warp is done with the item's list
-      if (kRes) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_LEMPTY + lb));
-      }
-    }
-    // end-of-work marker for the consumers
-    if (!*abort_flag && ptid == 0) {
-      mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-      ti[tik].item = -1;
-      ti[tik].n = 0;
-      ti[tik].flags = kFirst | kLast;
-      mbar_arrive(BAR(B_TIFULL + tik));
-    }
-    cp_async_wait_all();
-  } else if (warp == 4) {
-    // ====================================== MMA ========================================
-    if (lane == 0) {
-      // S: A = K rows (K-major), B = q rows (K-major).  O: A = V^T (MN-major), B = P^T (MN-major)
-      const uint32_t idS = kFp8 ? idesc_e4m3(128, 128, 0, 0) : idesc_bf16(128, 64, 0, 0);
-      const uint32_t idO = kFp8 ? idesc_e4m3(128, 64, 1, 1) : idesc_bf16(128, 64, 1, 1);
-      const uint32_t qbase = sb + kQOff, pbase = sb + kPOff;
-      int ring = 0, tik = 0, sbuf = 0;
-      uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
-      // S of a tile: A = K rows from the ring (K-major), B = q (K-major), into S buffer sbuf.
-      // Releases the K slots unless the tile is packed (V still to be read from them).
-      auto issue_s = [&](bool packed) -> bool {
-        if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) return false;
-        s_ph ^= 1u << sbuf;
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t dS = tmem + sbuf * M::kSCols;
-        for (int kc = 0; kc < n_chunks; ++kc) {
-          if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
-          for (int aa = 0; aa < 2; ++aa) {
-            const int atom = 2 * kc + aa;
-            if (atom >= n_atoms) break;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              if (atom * 4 + ks >= n_ks) break;
-              const uint64_t da = sdesc(slot + aa * kAtomBytes + ks * 32, 16, 1024);
-              const uint64_t db = sdesc(qbase + atom * M::kQAtom + ks * 32, 16, 1024);
-              if (kFp8)
-                mma_f8(dS, da, db, idS, (kc | aa | ks) != 0);
-              else
-                mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
-            }
-          }
-          if (!packed) mma_commit(BAR(B_EMPTY + ring));
-          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
-        }
-        mma_commit(BAR(B_SFULL + sbuf));
-        sbuf ^= 1;
-        return true;
-      };
-      // PV of a tile of n columns: A = V^T from the ring (MN-major), B = P^T (MN-major).
-      auto issue_pv = [&](int n, bool first, bool packed) -> bool {
-        if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) return false;
-        p_ph ^= 1;
-        if (first) {
-          if (!mbar_wait(BAR(B_OFREE), o_ph ^ 1, abort_flag)) return false;
-          o_ph ^= 1;
-        }
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t v_off = packed ? 64u * 128u : 0u;
-        for (int vc = 0; vc < n_chunks; ++vc) {
-          if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
-          if (!kFp8) {
-            // one 128-wide head_dim tile per slot (two 64-wide atoms, LBO apart); K = 16 columns
-            const uint32_t dO = tmem + M::kOCol + vc * 64;
-            const int nk = (n + 15) >> 4;
-            for (int kk = 0; kk < nk; ++kk) {
-              const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
-              const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
-              mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
-            }
-          } else {
-            // two 128-wide head_dim tiles per slot (one atom each); K = 32 columns; P^T is
-            // p_hi (64-byte rows, 64-byte swizzle) followed by p_lo, both into the same O
-            const int nk = (n + 31) >> 5;
-            for (int aa = 0; aa < 2; ++aa) {
-              const int mt = 2 * vc + aa;
-              if (mt >= n_mt) break;
-              const uint32_t dO = tmem + M::kOCol + mt * 64;
-              for (int kk = 0; kk < nk; ++kk) {
-                const uint64_t da = sdesc(slot + v_off + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
-                const uint64_t dh = sdesc64(pbase + kk * 2048, 8192, 512);
-                const uint64_t dl = sdesc64(pbase + 8192 + kk * 2048, 8192, 512);
-                mma_f8(dO, da, dh, idO, (first && kk == 0) ? 0u : 1u);
-                mma_f8(dO, da, dl, idO, 1u);
+              for (int k = 0; k < 8; ++k) {
+                sv[k] = sc[k];
+                const int idx = j * 128 + k * 16 + r0;
+                const int32_t code = idx < n ? lc[k] : -1;
+                if (code < 0) {
+                  sc[k] = nullptr;
+                } else {
+                  const uint8_t* base = (code >> kColPoolShift) ? p.rs.cmp.kv : p.rs.win.kv;
+                  sc[k] = base + (size_t)(code & ((1 << kColPoolShift) - 1)) * row_bytes;
+                }
               }
             }
+            nj_v = nj_c;
+            nj_c = min(128, n - j * 128);
           }
-          mma_commit(BAR(B_EMPTY + ring));
-          if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
-        }
-        mma_commit(BAR(B_PVDONE));
-        return true;
-      };
-      // Per item: S(0); then for every tile j: S(j + 1) (if any), PV(j).  The tile-info entry of
-      // the next tile is read before PV of the current one.
-      bool ok = true;
-      for (;;) {
-        if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
-        int n = ti[tik].n;
-        const int item = ti[tik].item;
-        int flags = ti[tik].flags;
-        mbar_arrive(BAR(B_TIEMPTY + tik));
-        if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-        if (item < 0) break;
-        if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;   // (every item begins a tile 0)
-        q_ph ^= 1;
-        if (n == 0) {  // an item without columns: hand the Q buffer back untouched
-          mma_commit(BAR(B_QEMPTY));
-          continue;
-        }
-        const bool packed = (flags & kLast) && n <= 64;   // a single packed tile
-        const int ring0 = ring;
-        const uint32_t ring_ph0 = ring_ph;
-        if (!(ok = issue_s(packed))) break;
-        if (flags & kLast) mma_commit(BAR(B_QEMPTY));
-        bool first = true;
-        for (;;) {
-          const bool last = flags & kLast;
-          int n_next = 0, flags_next = 0;
-          if (!last) {
-            if (!(ok = mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag))) break;
-            n_next = ti[tik].n;
-            flags_next = ti[tik].flags;
-            mbar_arrive(BAR(B_TIEMPTY + tik));
-            if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
-            if (!(ok = issue_s(false))) break;
-            if (flags_next & kLast) mma_commit(BAR(B_QEMPTY));
+          // V of the newest tile only at the very last step; otherwise V of the tile before it
+          const bool cur = half == 0 || st == n_steps - 1;
+          const int nj = cur ? nj_c : nj_v;
+          // Rows the MMAs read: the S MMA masks columns >= nj in the softmax, so K rows past nj
+          // may hold anything; the PV MMA reads V rows up to its K-step multiple, which must be
+          // finite past nj (zero probability times a stale NaN would still be NaN).
+          const int pv_step = kFp8 ? 32 : 16;
+          const int v_rows = (nj + pv_step - 1) / pv_step * pv_step;
+          if (tma) {
+            // Four rows per copy: K row groups over [0, nj) (the last one may repeat its first
+            // row), V row groups over [0, v_rows) (rows past nj repeat a row of the tile: finite
+            // values that meet zero probabilities).  A packed tile takes both, V at row 64.
+            // The gather warps work in pairs, fill f to pair f % (NG / 2), each of the two warps
+            // issuing up to 32 copies (one instruction) and arming the slot's barrier with their
+            // bytes: copies spread thinly over all warps issue far slower than full-warp batches.
+            const int32_t* tl = list + j * 128;
+            const int gk = half == 0 ? (nj + 3) >> 2 : 0;
+            const int gv = (half == 1 || packed) ? v_rows >> 2 : 0;
+            const int vrow0 = packed ? 64 : 0;
+            constexpr int rmask = (1 << kColPoolShift) - 1;
+            for (int kc = 0; kc < n_chunks; ++kc) {
+              if ((pw >> 1) == fills % (NG / 2)) {
+                const int na = min(2, n_atoms - 2 * kc);
+                const int ops = (gk + gv) * na;
+                const int half_ops = (ops + 1) >> 1;
+                const int o0 = (pw & 1) ? half_ops : 0;
+                const int mine = (pw & 1) ? ops - half_ops : half_ops;
+                bool okw = true;
+                if (lane == 0) okw = mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
+                okw = __shfl_sync(0xffffffffu, okw, 0);
+                const uint32_t full = BAR(B_FULL + ring);
+                if (lane == 0) mbar_arrive_expect_tx(full, okw ? (uint32_t)mine * 512u : 0u);
+                __syncwarp();
+                if (okw && lane < mine) {
+                  const int o = o0 + lane;
+                  const int gi = o / na, aa = o - gi * na;
+                  const bool isv = gi >= gk;
+                  const int r = 4 * (isv ? gi - gk : gi);   // first tile row of the group
+                  const int4 c4 = *reinterpret_cast<const int4*>(tl + r);
+                  int32_t code[4] = {c4.x, c4.y, c4.z, c4.w};
+                  const int32_t fill = r < nj ? code[0] : tl[0];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    if (r + i >= nj) code[i] = fill;
+                  const int pool = code[0] >> kColPoolShift;
+                  bool same = true;
+#pragma unroll
+                  for (int i = 1; i < 4; ++i) same = same && (code[i] >> kColPoolShift) == pool;
+                  const uint32_t dst = sb + kRingOff + ring * kSlotBytes + aa * kAtomBytes +
+                                       (uint32_t)((isv ? vrow0 : 0) + r) * 128u;
+                  const int x = (2 * kc + aa) * 128;
+                  const int mv = isv ? 1 : 0;
+                  if (same) {
+                    tma_gather4(dst, &p.kv_map[2 * pool + mv], x, code[0] & rmask, code[1] & rmask,
+                                code[2] & rmask, code[3] & rmask, full);
+                  } else {  // the group where the window rows end and the compressed rows begin
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                      tma_row(dst + 128u * i, &p.kv_map[2 * (code[i] >> kColPoolShift) + mv], x,
+                              code[i] & rmask, full);
+                  }
+                }
+              }
+              if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+              ++fills;
+            }
+            continue;
           }
-          if (packed) {  // PV reads the slots S just read
-            ring = ring0;
-            ring_ph = ring_ph0;
+          // Row groups of 16 past the rows the MMAs read are skipped with a warp-uniform test;
+          // V rows past nj are zero-filled.
+          const int kmax = ((half == 0 ? nj : v_rows) + 15) >> 4;
+          const int kmax_v = packed ? (v_rows + 15) >> 4 : 0;
+          const uint8_t* sr[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sr[k] = cur ? sc[k] : sv[k];
+          for (int kc = 0; kc < n_chunks; ++kc) {
+            if (ptid < 128) {   // cp.async copies: the first 128 gather threads
+              mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
+              const uint32_t d0 = sb + kRingOff + ring * kSlotBytes + dst_thread;
+              const bool a0 = (2 * kc) * 8 + jj < P16, a1 = (2 * kc + 1) * 8 + jj < P16;
+              const size_t so = (size_t)half * D * M::kElt + (size_t)(2 * kc) * 128 + jj * 16;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (k < kmax) {
+                  const uint8_t* sp = sr[k] ? sr[k] + so : p.q;
+                  const uint32_t sz = sr[k] ? 16u : 0u;
+                  if (a0) cp_async_16(d0 + k * 2048, sp, sz);
+                  if (a1) cp_async_16(d0 + kAtomBytes + k * 2048, sp + 128, sz);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (k < kmax_v) {
+                  const uint8_t* sp = sr[k] ? sr[k] + so + D * M::kElt : p.q;
+                  const uint32_t sz = sr[k] ? 16u : 0u;
+                  if (a0) cp_async_16(d0 + (4 + k) * 2048, sp, sz);
+                  if (a1) cp_async_16(d0 + kAtomBytes + (4 + k) * 2048, sp + 128, sz);
+                }
+              }
+              cp_async_arrive_noinc(BAR(B_FULL + ring));
+            }
+            if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+            ++fills;
           }
-          if (!(ok = issue_pv(n, first, packed))) break;
-          first = false;
-          if (last) break;
-          n = n_next;
-          flags = flags_next;
         }
-        if (!ok) break;
+        // this warp is done with the item's list
+        if (kRes) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LEMPTY + lb));
+        }
       }
-      // nothing may still write TMEM when it is released
-      mma_commit(BAR(B_DRAIN));
-      mbar_wait_drain(BAR(B_DRAIN), 0);
+      // end-of-work marker for the consumers
+      if (!*abort_flag && ptid == 0) {
+        mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+        ti[tik].item = -1;
+        ti[tik].n = 0;
+        ti[tik].flags = kFirst | kLast;
+        mbar_arrive(BAR(B_TIFULL + tik));
+      }
+      cp_async_wait_all();
+      if (tma && lane == 0) {
+        // Tensor-map copies land asynchronously: before this CTA can end, the last fill of every
+        // slot must have completed (at once after a normal run, whose MMAs consumed them all; an
+        // aborted run may wait out the drain limit).  Fill f went to slot f % 4, barrier phase f / 4.
+        for (int sl = 0; sl < kStages && sl < fills; ++sl) {
+          const int f = fills - 1 - ((fills - 1 - sl) % kStages);
+          mbar_wait_drain(BAR(B_FULL + sl), (uint32_t)((f / kStages) & 1));
+        }
+      }
+    } else if (warp == 4) {
+      // ====================================== MMA ========================================
+      if (lane == 0) {
+        // S: A = K rows (K-major), B = q rows (K-major).  O: A = V^T (MN-major), B = P^T (MN-major)
+        const uint32_t idS = kFp8 ? idesc_e4m3(128, 128, 0, 0) : idesc_bf16(128, 64, 0, 0);
+        const uint32_t idO = kFp8 ? idesc_e4m3(128, 64, 1, 1) : idesc_bf16(128, 64, 1, 1);
+        const uint32_t qbase = sb + kQOff, pbase = sb + kPOff;
+        int ring = 0, tik = 0, sbuf = 0;
+        uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0, s_ph = 0, p_ph = 0, o_ph = 0;
+        // S of a tile: A = K rows from the ring (K-major), B = q (K-major), into S buffer sbuf.
+        // Releases the K slots unless the tile is packed (V still to be read from them).
+        auto issue_s = [&](bool packed) -> bool {
+          if (!mbar_wait(BAR(B_SEMPTY + sbuf), ((s_ph >> sbuf) & 1u) ^ 1u, abort_flag)) return false;
+          s_ph ^= 1u << sbuf;
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t dS = tmem + sbuf * M::kSCols;
+          for (int kc = 0; kc < n_chunks; ++kc) {
+            if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+            for (int aa = 0; aa < 2; ++aa) {
+              const int atom = 2 * kc + aa;
+              if (atom >= n_atoms) break;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                if (atom * 4 + ks >= n_ks) break;
+                const uint64_t da = sdesc(slot + aa * kAtomBytes + ks * 32, 16, 1024);
+                const uint64_t db = sdesc(qbase + atom * M::kQAtom + ks * 32, 16, 1024);
+                if (kFp8)
+                  mma_f8(dS, da, db, idS, (kc | aa | ks) != 0);
+                else
+                  mma_bf16(dS, da, db, idS, (kc | aa | ks) != 0);
+              }
+            }
+            if (!packed) mma_commit(BAR(B_EMPTY + ring));
+            if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+          }
+          mma_commit(BAR(B_SFULL + sbuf));
+          sbuf ^= 1;
+          return true;
+        };
+        // PV of a tile of n columns: A = V^T from the ring (MN-major), B = P^T (MN-major).
+        auto issue_pv = [&](int n, bool first, bool packed) -> bool {
+          if (!mbar_wait(BAR(B_PFULL), p_ph, abort_flag)) return false;
+          p_ph ^= 1;
+          if (first) {
+            if (!mbar_wait(BAR(B_OFREE), o_ph ^ 1, abort_flag)) return false;
+            o_ph ^= 1;
+          }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t v_off = packed ? 64u * 128u : 0u;
+          for (int vc = 0; vc < n_chunks; ++vc) {
+            if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+            if (!kFp8) {
+              // one 128-wide head_dim tile per slot (two 64-wide atoms, LBO apart); K = 16 columns
+              const uint32_t dO = tmem + M::kOCol + vc * 64;
+              const int nk = (n + 15) >> 4;
+              for (int kk = 0; kk < nk; ++kk) {
+                const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
+                const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+                mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
+              }
+            } else {
+              // two 128-wide head_dim tiles per slot (one atom each); K = 32 columns; P^T is
+              // p_hi (64-byte rows, 64-byte swizzle) followed by p_lo, both into the same O
+              const int nk = (n + 31) >> 5;
+              for (int aa = 0; aa < 2; ++aa) {
+                const int mt = 2 * vc + aa;
+                if (mt >= n_mt) break;
+                const uint32_t dO = tmem + M::kOCol + mt * 64;
+                for (int kk = 0; kk < nk; ++kk) {
+                  const uint64_t da = sdesc(slot + v_off + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
+                  const uint64_t dh = sdesc64(pbase + kk * 2048, 8192, 512);
+                  const uint64_t dl = sdesc64(pbase + 8192 + kk * 2048, 8192, 512);
+                  mma_f8(dO, da, dh, idO, (first && kk == 0) ? 0u : 1u);
+                  mma_f8(dO, da, dl, idO, 1u);
+                }
+              }
+            }
+            mma_commit(BAR(B_EMPTY + ring));
+            if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+          }
+          mma_commit(BAR(B_PVDONE));
+          return true;
+        };
+        // Per item: S(0); then for every tile j: S(j + 1) (if any), PV(j).  The tile-info entry of
+        // the next tile is read before PV of the current one.
+        bool ok = true;
+        for (;;) {
+          if (!mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag)) break;
+          int n = ti[tik].n;
+          const int item = ti[tik].item;
+          int flags = ti[tik].flags;
+          mbar_arrive(BAR(B_TIEMPTY + tik));
+          if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+          if (item < 0) break;
+          if (!mbar_wait(BAR(B_QFULL), q_ph, abort_flag)) break;   // (every item begins a tile 0)
+          q_ph ^= 1;
+          if (n == 0) {  // an item without columns: hand the Q buffer back untouched
+            mma_commit(BAR(B_QEMPTY));
+            continue;
+          }
+          const bool packed = (flags & kLast) && n <= 64;   // a single packed tile
+          const int ring0 = ring;
+          const uint32_t ring_ph0 = ring_ph;
+          if (!(ok = issue_s(packed))) break;
+          if (flags & kLast) mma_commit(BAR(B_QEMPTY));
+          bool first = true;
+          for (;;) {
+            const bool last = flags & kLast;
+            int n_next = 0, flags_next = 0;
+            if (!last) {
+              if (!(ok = mbar_wait(BAR(B_TIFULL + tik), ti_ph, abort_flag))) break;
+              n_next = ti[tik].n;
+              flags_next = ti[tik].flags;
+              mbar_arrive(BAR(B_TIEMPTY + tik));
+              if (++tik == kTi) { tik = 0; ti_ph ^= 1; }
+              if (!(ok = issue_s(false))) break;
+              if (flags_next & kLast) mma_commit(BAR(B_QEMPTY));
+            }
+            if (packed) {  // PV reads the slots S just read
+              ring = ring0;
+              ring_ph = ring_ph0;
+            }
+            if (!(ok = issue_pv(n, first, packed))) break;
+            first = false;
+            if (last) break;
+            n = n_next;
+            flags = flags_next;
+          }
+          if (!ok) break;
+        }
+        // nothing may still write TMEM when it is released
+        mma_commit(BAR(B_DRAIN));
+        mbar_wait_drain(BAR(B_DRAIN), 0);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ================================ softmax / epilogue ================================
     const int tid = threadIdx.x;  // column of the tile == TMEM lane
@@ -1210,9 +1302,7 @@ __global__ void __launch_bounds__(kRes ? cfg::kThreads : cfg::kThreads - 32, 1)
         }
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
-          float inv[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) inv[k] = arow[hf * 32 + k];
+          const float* inv = arow + hf * 32;   // 1 / denominator of each head of this half
           const size_t row0 = (size_t)t * p.H + g * p.gh + hf * 32;  // first head of this half
           const int nh = min(32, Hg - hf * 32);                     // heads of this half present
 #pragma unroll 1
@@ -1335,19 +1425,28 @@ __global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ c
 }
 
 namespace {
-template <bool kFp8, bool kRes>
-const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(attn_kernel<kFp8, kRes>);
+// the kernel variants: e4m3 (cp.async, with or without resolver); bf16 by cp.async (one item per
+// CTA, no resolver) or by tensor-map gathers (with or without resolver)
+constexpr int kVariants = 5;
+const void* attn_kernel_ptr(int v) {
+  switch (v) {
+    case 0: return reinterpret_cast<const void*>(attn_kernel<true, false, false>);
+    case 1: return reinterpret_cast<const void*>(attn_kernel<true, true, false>);
+    case 2: return reinterpret_cast<const void*>(attn_kernel<false, false, false>);
+    case 3: return reinterpret_cast<const void*>(attn_kernel<false, false, true>);
+    default: return reinterpret_cast<const void*>(attn_kernel<false, true, true>);
+  }
 }
-const void* attn_kernel_ptr(bool fp8, bool res) {
-  if (fp8) return res ? kernel_ptr<true, true>() : kernel_ptr<true, false>();
-  return res ? kernel_ptr<false, true>() : kernel_ptr<false, false>();
+int attn_variant(bool fp8, bool res, bool tma) {
+  if (fp8) return res ? 1 : 0;
+  if (!tma) return 2;
+  return res ? 4 : 3;
 }
 }  // namespace
 
 cudaError_t prepare_attn_kernels() {
-  for (int f = 0; f < 4; ++f) {
-    const void* k = attn_kernel_ptr(f & 1, f & 2);
+  for (int f = 0; f < kVariants; ++f) {
+    const void* k = attn_kernel_ptr(f);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -1360,10 +1459,10 @@ cudaError_t prepare_attn_kernels() {
 
 namespace {
 cudaLaunchConfig_t attn_config(int grid, int cluster, cudaStream_t stream,
-                               cudaLaunchAttribute* attr, bool res) {
+                               cudaLaunchAttribute* attr, bool tma, bool res) {
   cudaLaunchConfig_t c = {};
   c.gridDim = dim3((unsigned)grid, 1, 1);
-  c.blockDim = dim3(res ? cfg::kThreads : cfg::kThreads - 32, 1, 1);
+  c.blockDim = dim3((unsigned)attn_threads(tma, res), 1, 1);
   c.dynamicSmemBytes = cfg::kSmemBytes;
   c.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1377,11 +1476,12 @@ cudaLaunchConfig_t attn_config(int grid, int cluster, cudaStream_t stream,
 }  // namespace
 
 int attn_max_active_clusters(int cluster, bool fp8) {
-  // cluster launches give every CTA one item: the kernel without the resolver warp
+  // cluster launches give every CTA one item: the cp.async kernel without the resolver warp
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t c = attn_config(cluster, cluster, nullptr, attr, false);
+  cudaLaunchConfig_t c = attn_config(cluster, cluster, nullptr, attr, false, false);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel_ptr(fp8, false), &c) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_kernel_ptr(attn_variant(fp8, false, false)), &c) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1393,13 +1493,16 @@ cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t st
   // a resolver warp pays off when CTAs have more than one item and the column sets are long
   // enough that walking the page tables is a real share of an item (a single window tile is not)
   const bool res = grid < p.n_items && p.rs.W + p.rs.K >= 256;
-  cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr, res);
-  if (fp8) {
-    if (res) return cudaLaunchKernelEx(&c, attn_kernel<true, true>, p);
-    return cudaLaunchKernelEx(&c, attn_kernel<true, false>, p);
+  // tensor-map gathers for bf16 CTAs with more than one item
+  const bool tma = !fp8 && grid < p.n_items;
+  cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr, tma, res);
+  switch (attn_variant(fp8, res, tma)) {
+    case 0: return cudaLaunchKernelEx(&c, attn_kernel<true, false, false>, p);
+    case 1: return cudaLaunchKernelEx(&c, attn_kernel<true, true, false>, p);
+    case 2: return cudaLaunchKernelEx(&c, attn_kernel<false, false, false>, p);
+    case 3: return cudaLaunchKernelEx(&c, attn_kernel<false, false, true>, p);
+    default: return cudaLaunchKernelEx(&c, attn_kernel<false, true, true>, p);
   }
-  if (res) return cudaLaunchKernelEx(&c, attn_kernel<false, true>, p);
-  return cudaLaunchKernelEx(&c, attn_kernel<false, false>, p);
 }
 
 int merge_max_splits() { return kMergeMaxSplits; }

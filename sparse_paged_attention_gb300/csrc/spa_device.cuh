@@ -3,6 +3,7 @@
 // page-table resolution shared by the attention kernels and the column dump.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "sparse_attn_paged.h"
@@ -272,6 +273,29 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 // increment: the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Tensor-map row copies into shared memory (the map's box is 128 bytes of one row, 128-byte
+// swizzle; the swizzle follows the destination address, so a row may land at any 128-byte line of
+// a 1024-byte-aligned atom).  Completion: `bytes` of the barrier's transaction count.
+//   tma_gather4: four rows (any row indices of the map) to four consecutive 128-byte lines.
+//   tma_row:     one row.
+// x is the byte offset within the row (a multiple of 128 here).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_row(uint32_t dst, const CUtensorMap* map, int x, int r,
+                                        uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void cp_async_wait_all() {

@@ -8,6 +8,10 @@
 namespace spa {
 
 struct AttnParams {
+  // Tensor maps of the bf16 pools' rows: K rows of the window pool, its V rows, then the same for
+  // the compressed pool.  Each is a 2D byte tensor, one row per token (2*D bytes, row stride 4*D:
+  // K and V interleave), 128-byte boxes one row high, 128-byte swizzle.  Unused for e4m3.
+  CUtensorMap kv_map[4];
   ResolveArgs rs;
   const uint8_t* q;     // bf16 [T][H][D]
   uint8_t* out;         // bf16 [T][H][D] (prefill)
@@ -25,8 +29,14 @@ struct AttnParams {
                         // cluster and merge their partials through distributed shared memory
 };
 
-// Kernel launch configuration.
-constexpr int kAttnThreads = 320;     // 4 softmax, 1 MMA, 4 gather warps, 1 resolver warp
+// Kernel launch configuration: 4 softmax warps, 1 MMA warp, the gather warps and 1 resolver
+// warp when CTAs have more than one item.  6 gather warps when rows move by tensor-map gathers
+// (their issue rate grows with the warps issuing them; 12 warps in all keep 168 registers a
+// thread), 4 when they move by cp.async.
+__host__ __device__ constexpr int attn_gather_warps(bool tma) { return tma ? 6 : 4; }
+__host__ __device__ constexpr int attn_threads(bool tma, bool res) {
+  return 32 * (5 + attn_gather_warps(tma) + (res ? 1 : 0));
+}
 int attn_smem_bytes();
 constexpr int kMaxColumns = 1024;     // window + top-k columns per query
 
