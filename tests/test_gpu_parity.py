@@ -182,6 +182,28 @@ def test_edge_cases(case, mode):
     assert np.array_equal(cols, oracle_columns(w)[0])
 
 
+# The same shapes with more queries than SMs: CTAs then take several items, and bf16 rows move by
+# tensor-map gathers (four rows a copy; a group of four that straddles the end of the window
+# rows, as in the first queries of a sequence, goes row by row).  Sampled queries: the first
+# positions (ragged windows), tile edges, and the tokens of the other sequences.
+MANY_SAMPLE = [0, 1, 2, 3, 5, 7, 11, 31, 63, 64, 65, 127, 128, 129, 190, 199, 200, 201, 202]
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_cases_many_items(case):
+    kw = dict(EDGE[case])
+    kw.setdefault("page_size", 16)
+    seqs = [np.arange(0, 200), np.array([2, 999]), np.array([4095])]
+    w = build(case, seq_positions=seqs, seed=9, **kw)
+    d = OnDevice(w, _dev())
+    out = d.prefill()
+    check_no_device_error()
+    ref, _, _, err = run_oracle(w, tokens=np.array(MANY_SAMPLE))
+    assert not err
+    compare(out, ref, tokens=np.array(MANY_SAMPLE), gate=REL_MEAN_GATE_BF16,
+            what=f"{case} prefill, several items per CTA")
+
+
 def test_bad_block_id_is_reported_and_dropped():
     w = build("bad", seq_positions=[np.array([40, 41])], num_heads=8, head_dim=64, window=8,
               topk=8, ratio=4, page_size=4, seed=3)
