@@ -93,13 +93,13 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// K rows (v = 0) or V rows (v = 1) of a pool [num_blocks][page_size][2][D] bf16 as a 2D byte
-// tensor: row i = token row i of the pool (2*D bytes), row stride 4*D bytes.  Boxes are 128 bytes
-// of one row; the 128-byte swizzle puts them straight into the MMA operand layout.
-bool encode_pool_rows(CUtensorMap* m, const spa_pool_t* pl, int D, int v) {
+// K rows (v = 0) or V rows (v = 1) of a pool [num_blocks][page_size][2][D] (elt bytes each) as a
+// 2D byte tensor: row i = token row i of the pool (D*elt bytes), row stride 2*D*elt bytes.  Boxes
+// are 128 bytes of one row; the 128-byte swizzle puts them straight into the MMA operand layout.
+bool encode_pool_rows(CUtensorMap* m, const spa_pool_t* pl, int D, int elt, int v) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
-  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  const cuuint64_t row_bytes = (cuuint64_t)D * elt;
   const cuuint64_t rows = (cuuint64_t)pl->num_blocks * (cuuint64_t)pl->page_size;
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {2 * row_bytes};
@@ -115,22 +115,24 @@ bool encode_pool_rows(CUtensorMap* m, const spa_pool_t* pl, int D, int v) {
 struct PoolMaps {
   const void* kv = nullptr;
   long long num_blocks = 0;
-  int page_size = 0, D = 0;
+  int page_size = 0, D = 0, elt = 0;
   CUtensorMap map[2];
 };
 thread_local PoolMaps g_maps[2];
 
-bool pool_maps(CUtensorMap* out, const spa_pool_t* pl, int D, int which) {
+bool pool_maps(CUtensorMap* out, const spa_pool_t* pl, int D, int elt, int which) {
   PoolMaps& c = g_maps[which];
   if (c.kv != pl->kv || c.num_blocks != pl->num_blocks || c.page_size != pl->page_size ||
-      c.D != D) {
+      c.D != D || c.elt != elt) {
     c.kv = nullptr;
-    if (!encode_pool_rows(&c.map[0], pl, D, 0) || !encode_pool_rows(&c.map[1], pl, D, 1))
+    if (!encode_pool_rows(&c.map[0], pl, D, elt, 0) ||
+        !encode_pool_rows(&c.map[1], pl, D, elt, 1))
       return false;
     c.kv = pl->kv;
     c.num_blocks = pl->num_blocks;
     c.page_size = pl->page_size;
     c.D = D;
+    c.elt = elt;
   }
   out[0] = c.map[0];
   out[1] = c.map[1];
@@ -316,9 +318,11 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   p.n_items = (int)items;
   // clustered: one item per CTA; otherwise a persistent grid of at most one CTA per SM
   const int grid = p.cluster > 1 ? (int)items : (int)(items < sms ? items : sms);
-  if (!fp8 && grid < items) {  // CTAs with several items gather bf16 rows by tensor maps
-    if (!pool_maps(&p.kv_map[0], win, pr->head_dim, 0)) return SPA_ERR_CUDA;
-    if (!pool_maps(&p.kv_map[2], uses_cmp(pr) ? cmp : win, pr->head_dim, 1)) return SPA_ERR_CUDA;
+  if (spa::attn_uses_tma(grid, items, fp8, pr->head_dim)) {
+    const int elt = fp8 ? 1 : 2;
+    if (!pool_maps(&p.kv_map[0], win, pr->head_dim, elt, 0)) return SPA_ERR_CUDA;
+    if (!pool_maps(&p.kv_map[2], uses_cmp(pr) ? cmp : win, pr->head_dim, elt, 1))
+      return SPA_ERR_CUDA;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = spa::launch_attn(p, grid, fp8, s);

@@ -228,14 +228,14 @@ __device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t lbo, uint32
 
 // kRes: a resolver warp (the last) walks the page tables of a CTA's next item while the gather
 // warps copy the current one; launched only when CTAs have more than one item.
-// kTma: bf16 rows move by tensor-map gathers (CTAs with many items: throughput); otherwise by
-// cp.async, whose lower issue latency suits CTAs of a single item (decode) and e4m3 rows.
+// kTma: K/V rows move by tensor-map gathers (CTAs with many items: throughput); otherwise by
+// cp.async, whose lower issue latency suits CTAs of a single item (decode), and which also takes
+// e4m3 rows of a head_dim that is not a multiple of 128.
 template <bool kFp8, bool kRes, bool kTma>
 __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
     attn_kernel(const __grid_constant__ AttnParams p) {
   using namespace cfg;
   using M = Mode<kFp8, kTma>;
-  static_assert(!(kFp8 && kTma), "e4m3 rows are copied by cp.async");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -373,7 +373,6 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
     } else if (warp >= 5 && warp < 5 + M::kNG) {
       // ===================================== gather ======================================
       constexpr int NG = M::kNG, NGT = M::kNGT;
-      static_assert(!kFp8 || NG == 4, "the e4m3 path's per-column work assumes 128 gather threads");
       static_assert(!M::kTma || NG % 2 == 0, "tensor-map gathers run in pairs of warps");
       const int ptid = threadIdx.x - 160;
       const int pw = warp - 5;
@@ -387,6 +386,9 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
       int ring = 0, tik = 0;
       uint32_t ring_ph = 0, ti_ph = 0, q_ph = 0;
       int fills = 0;  // ring slots this thread has filled
+      // threads that write a tile-info entry: thread 0, and for e4m3 the first 128 (per-column
+      // K and V scales)
+      const bool ti_writer = kFp8 ? ptid < 128 : ptid == 0;
       int32_t* lists = reinterpret_cast<int32_t*>(sm + kListOff);
       const ItemInfo* info = reinterpret_cast<const ItemInfo*>(sm + kInfoOff);
       for (int u = 0;; ++u) {
@@ -446,7 +448,9 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
             vmax = warp_max(vmax);
             if (lane == 0) fred[pw] = vmax;
             named_bar_sync(2, NGT);
-            vmax = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
+            vmax = 0.f;
+#pragma unroll
+            for (int w = 0; w < NG; ++w) vmax = fmaxf(vmax, fred[w]);
             named_bar_sync(2, NGT);
             // probabilities are <= 2^tau, so P * v_scale * p_scale stays <= 448
             p_scale = vmax > 0.f ? pow2_floor(448.f / (exp2f(M::kTau) * vmax)) : 1.f;
@@ -488,9 +492,9 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
               if (pass == 1) {
                 qm = warp_max(qm);
                 if (lane == 0) fred[pw] = qm;
-                named_bar_sync(2, 128);
+                named_bar_sync(3, 128);   // (barrier 3: the first 128 gather threads)
                 qm = fmaxf(fmaxf(fred[0], fred[1]), fmaxf(fred[2], fred[3]));
-                named_bar_sync(2, 128);
+                named_bar_sync(3, 128);
                 q_scale = qm > 0.f ? pow2_floor(448.f / qm) : 1.f;
               }
               // four pieces per round, their eight 16-byte loads in flight together
@@ -556,11 +560,11 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         int nj_c = 0, nj_v = 0;
         if (n == 0) {
           // no column: one tile-info entry tells the consumers
-          if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-          if (kFp8) {
+          if (ti_writer) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+          if (kFp8 && ptid < 128) {
             ti[tik].k_scale[ptid] = 0.f;
             ti[tik].v_scale[ptid] = 0.f;
-            named_bar_sync(2, 128);
+            named_bar_sync(3, 128);
           }
           if (ptid == 0) {
             TileInfo& e = ti[tik];
@@ -585,8 +589,8 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
             // wait for it to be free, and all of them have seen it free before it is published:
             // a thread that waited without taking part could look only after the consumers had
             // freed the entry's next use too, and then wait on a parity that never comes back.
-            if (kFp8 || ptid == 0) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
-            if (kFp8) {
+            if (ti_writer) mbar_wait(BAR(B_TIEMPTY + tik), ti_ph ^ 1, abort_flag);
+            if (kFp8 && ptid < 128) {
               const int idx = j * 128 + ptid;
               const int32_t code = idx < n ? list[list_pos(idx, tma)] : -1;
               float ks = 0.f, vs = 0.f;
@@ -598,7 +602,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
               }
               ti[tik].k_scale[ptid] = ks;
               ti[tik].v_scale[ptid] = vs;
-              named_bar_sync(2, 128);
+              named_bar_sync(3, 128);
             }
             if (ptid == 0) {
               TileInfo& e = ti[tik];
@@ -1425,21 +1429,23 @@ __global__ void resolve_dump_kernel(const ResolveArgs a, int32_t* __restrict__ c
 }
 
 namespace {
-// the kernel variants: e4m3 (cp.async, with or without resolver); bf16 by cp.async (one item per
-// CTA, no resolver) or by tensor-map gathers (with or without resolver)
-constexpr int kVariants = 5;
+// the kernel variants: rows by cp.async (one item per CTA, or e4m3 rows of a head_dim that is
+// not a multiple of 128) or by tensor-map gathers, with or without the resolver warp
+constexpr int kVariants = 7;
 const void* attn_kernel_ptr(int v) {
   switch (v) {
     case 0: return reinterpret_cast<const void*>(attn_kernel<true, false, false>);
     case 1: return reinterpret_cast<const void*>(attn_kernel<true, true, false>);
     case 2: return reinterpret_cast<const void*>(attn_kernel<false, false, false>);
     case 3: return reinterpret_cast<const void*>(attn_kernel<false, false, true>);
-    default: return reinterpret_cast<const void*>(attn_kernel<false, true, true>);
+    case 4: return reinterpret_cast<const void*>(attn_kernel<false, true, true>);
+    case 5: return reinterpret_cast<const void*>(attn_kernel<true, false, true>);
+    default: return reinterpret_cast<const void*>(attn_kernel<true, true, true>);
   }
 }
 int attn_variant(bool fp8, bool res, bool tma) {
-  if (fp8) return res ? 1 : 0;
-  if (!tma) return 2;
+  if (fp8) return tma ? (res ? 6 : 5) : (res ? 1 : 0);
+  if (!tma) return 2;   // (bf16 by cp.async only for one item per CTA: no resolver)
   return res ? 4 : 3;
 }
 }  // namespace
@@ -1493,15 +1499,16 @@ cudaError_t launch_attn(const AttnParams& p, int grid, bool fp8, cudaStream_t st
   // a resolver warp pays off when CTAs have more than one item and the column sets are long
   // enough that walking the page tables is a real share of an item (a single window tile is not)
   const bool res = grid < p.n_items && p.rs.W + p.rs.K >= 256;
-  // tensor-map gathers for bf16 CTAs with more than one item
-  const bool tma = !fp8 && grid < p.n_items;
+  const bool tma = attn_uses_tma(grid, p.n_items, fp8, p.D);
   cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr, tma, res);
   switch (attn_variant(fp8, res, tma)) {
     case 0: return cudaLaunchKernelEx(&c, attn_kernel<true, false, false>, p);
     case 1: return cudaLaunchKernelEx(&c, attn_kernel<true, true, false>, p);
     case 2: return cudaLaunchKernelEx(&c, attn_kernel<false, false, false>, p);
     case 3: return cudaLaunchKernelEx(&c, attn_kernel<false, false, true>, p);
-    default: return cudaLaunchKernelEx(&c, attn_kernel<false, true, true>, p);
+    case 4: return cudaLaunchKernelEx(&c, attn_kernel<false, true, true>, p);
+    case 5: return cudaLaunchKernelEx(&c, attn_kernel<true, false, true>, p);
+    default: return cudaLaunchKernelEx(&c, attn_kernel<true, true, true>, p);
   }
 }
 

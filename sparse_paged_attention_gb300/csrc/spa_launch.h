@@ -8,9 +8,10 @@
 namespace spa {
 
 struct AttnParams {
-  // Tensor maps of the bf16 pools' rows: K rows of the window pool, its V rows, then the same for
-  // the compressed pool.  Each is a 2D byte tensor, one row per token (2*D bytes, row stride 4*D:
-  // K and V interleave), 128-byte boxes one row high, 128-byte swizzle.  Unused for e4m3.
+  // Tensor maps of the pools' rows: K rows of the window pool, its V rows, then the same for the
+  // compressed pool.  Each is a 2D byte tensor, one row per token (D elements, the row stride
+  // twice that: K and V interleave), 128-byte boxes one row high, 128-byte swizzle.  Set only
+  // for launches that gather rows by tensor maps.
   CUtensorMap kv_map[4];
   ResolveArgs rs;
   const uint8_t* q;     // bf16 [T][H][D]
@@ -36,6 +37,11 @@ struct AttnParams {
 __host__ __device__ constexpr int attn_gather_warps(bool tma) { return tma ? 6 : 4; }
 __host__ __device__ constexpr int attn_threads(bool tma, bool res) {
   return 32 * (5 + attn_gather_warps(tma) + (res ? 1 : 0));
+}
+// Rows move by tensor-map gathers when CTAs take more than one item (throughput) and a row is a
+// whole number of 128-byte boxes; otherwise by cp.async.
+inline bool attn_uses_tma(long long grid, long long n_items, bool fp8, int head_dim) {
+  return grid < n_items && (head_dim * (fp8 ? 1 : 2)) % 128 == 0;
 }
 int attn_smem_bytes();
 constexpr int kMaxColumns = 1024;     // window + top-k columns per query

@@ -282,3 +282,20 @@ def test_fp8_cases(case, mode):
     ref, _, _, err = run_oracle(w)
     assert not err
     compare(out, ref, gate=REL_MEAN_GATE_FP8, what=f"{case} {mode}")
+
+
+@pytest.mark.parametrize("case", sorted(c for c in FP8_EDGE if c != "fp8_decode_b1"))
+def test_fp8_cases_many_items(case):
+    """e4m3 pools with more queries than SMs: tensor-map gathers where a row is a whole number of
+    128-byte boxes (head_dim 256, 512), cp.async with a resolver warp otherwise (64, 192)."""
+    kw = dict(FP8_EDGE[case])
+    kw.setdefault("page_size", 16)
+    seqs = [np.arange(0, 200), np.array([2, 999]), np.array([4095])]
+    w = build(case, seq_positions=seqs, seed=13, fp8=True, **kw)
+    d = OnDevice(w, _dev())
+    out = d.prefill()
+    check_no_device_error()
+    ref, _, _, err = run_oracle(w, tokens=np.array(MANY_SAMPLE))
+    assert not err
+    compare(out, ref, tokens=np.array(MANY_SAMPLE), gate=REL_MEAN_GATE_FP8,
+            what=f"{case} prefill, several items per CTA")
