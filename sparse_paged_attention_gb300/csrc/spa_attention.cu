@@ -80,6 +80,7 @@ static_assert(sizeof(TileInfo) % 16 == 0, "tile info alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr int kFirst = 1, kLast = 2;
+constexpr int kTmaFillWarps = 2;      // gather warps that issue one ring fill together
 }  // namespace cfg
 
 template <bool kFp8, bool kTmaRows>
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
     for (int i = 0; i < kStages; ++i) {
       // tensor maps: the armed arrivals of the pair of gather warps that fills the slot;
       // cp.async: the noinc arrivals of the first 128 gather threads
-      mbar_init(BAR(B_FULL + i), M::kTma ? 2 : 128);
+      mbar_init(BAR(B_FULL + i), M::kTma ? kTmaFillWarps : 128);
       mbar_init(BAR(B_EMPTY + i), 1);
     }
     mbar_init(BAR(B_QFULL), 128);
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
     } else if (warp >= 5 && warp < 5 + M::kNG) {
       // ===================================== gather ======================================
       constexpr int NG = M::kNG, NGT = M::kNGT;
-      static_assert(!M::kTma || NG % 2 == 0, "tensor-map gathers run in pairs of warps");
+      static_assert(!M::kTma || NG % kTmaFillWarps == 0, "tensor-map gathers run in warp groups");
       const int ptid = threadIdx.x - 160;
       const int pw = warp - 5;
       volatile int* cnt = reinterpret_cast<volatile int*>(sm + kCntOff);            // [16]
@@ -656,13 +657,14 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
             const int gv = (half == 1 || packed) ? v_rows >> 2 : 0;
             const int vrow0 = packed ? 64 : 0;
             constexpr int rmask = (1 << kColPoolShift) - 1;
+            constexpr int kFillWarps = kTmaFillWarps;
             for (int kc = 0; kc < n_chunks; ++kc) {
-              if ((pw >> 1) == fills % (NG / 2)) {
+              if (pw / kFillWarps == fills % (NG / kFillWarps)) {
                 const int na = min(2, n_atoms - 2 * kc);
                 const int ops = (gk + gv) * na;
-                const int half_ops = (ops + 1) >> 1;
-                const int o0 = (pw & 1) ? half_ops : 0;
-                const int mine = (pw & 1) ? ops - half_ops : half_ops;
+                const int per = (ops + kFillWarps - 1) / kFillWarps;
+                const int o0 = (pw % kFillWarps) * per;
+                const int mine = max(0, min(per, ops - o0));
                 bool okw = true;
                 if (lane == 0) okw = mbar_wait(BAR(B_EMPTY + ring), ring_ph ^ 1, abort_flag);
                 okw = __shfl_sync(0xffffffffu, okw, 0);
