@@ -1183,17 +1183,20 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        // lane k of warp 0 sends to CTA k: first every (m, l) block, then the row slices, so the
-        // small copies are not queued behind the large ones
+        // lane l of warp w sends to CTA k = 4l + w: first its (m, l) block, then its row slice,
+        // so the small copies are not queued behind the large ones.  A warp's copies issue one
+        // after the other, so the sends are spread over the four warps.
         const uint32_t recv_ml = sb + kRingOff + (uint32_t)(D * rb_bytes);
         const bool send = ok && __shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0) != 0;
-        if (warp == 0 && lane < S && send) {   // (the same lanes on both sides of the warp sync)
-          const uint32_t k = (uint32_t)lane;
+        const int k_to = 4 * lane + warp;
+        const int senders = warp < S ? (S - warp + 3) >> 2 : 0;   // lanes of this warp that send
+        if (k_to < S && send) {   // (the same lanes on both sides of the warp sync)
+          const uint32_t k = (uint32_t)k_to;
           const bool go = mbar_wait_cluster(BAR(B_READY), 0, abort_flag);
           if (go)
             bulk_copy_cluster(mapa_cluster(recv_ml + rank * ml_bytes, k), sb + kPOff, ml_bytes,
                               mapa_cluster(BAR(B_RECVML), k));
-          __syncwarp((1u << S) - 1u);
+          __syncwarp((1u << senders) - 1u);
           if (go)
             bulk_copy_cluster(mapa_cluster(sb + kRingOff + rank * dpo * rb_bytes, k),
                               sb + kQOff + (uint32_t)(k * dpo * rb_bytes), dpo * rb_bytes,
@@ -1347,8 +1350,9 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
   }
   if (clustered) {
     // no CTA leaves while a peer may still read or write its shared memory
+    // (a relaxed arrival: this barrier orders no data, every copy between the CTAs was waited for)
     if (!cl_started) cluster_wait();
-    cluster_arrive();
+    cluster_arrive_relaxed();
     cluster_wait();
     // after a failed merge, copies from peers may still be landing here: let them finish
     if (threadIdx.x == 0 && !recv_ok) {
