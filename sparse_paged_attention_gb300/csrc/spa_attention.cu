@@ -977,7 +977,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         const uint32_t s_addr = lane_base + sbuf * M::kSCols;
         float* rr = red + rb * 256;
         // pass 1: tile maximum of every head (lane L ends up with heads L and 32 + L)
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
           tmem_ld32(s_addr + hf * 32, x);
@@ -1026,7 +1026,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         if (grow && !first) {
           // the running max moved: rescale O
           for (int i = 0; i < n_mt; ++i) {
-#pragma unroll
+#pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
               float o[32];
               const uint32_t ta = lane_base + M::kOCol + i * 64 + hf * 32;
@@ -1042,7 +1042,7 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         l0 *= a0;
         l1 *= a1;
         // pass 2: probabilities, P^T row of this column, this warp's denominators
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
           tmem_ld32(s_addr + hf * 32, x);
