@@ -821,6 +821,27 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t v_off = packed ? 64u * 128u : 0u;
+          if (!kFp8 && packed) {
+            // A packed tile's slots were waited for by its S just before: issue the MMAs of all
+            // head_dim tiles back to back (interleaved, no per-slot wait), then release the slots.
+            const int nk = (n + 15) >> 4;
+            for (int kk = 0; kk < nk; ++kk) {
+              const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+              int r = ring;
+              for (int vc = 0; vc < n_chunks; ++vc) {
+                const uint32_t slot = sb + kRingOff + r * kSlotBytes;
+                const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
+                mma_bf16(tmem + M::kOCol + vc * 64, da, db, idO, (first && kk == 0) ? 0u : 1u);
+                if (++r == kStages) r = 0;
+              }
+            }
+            for (int vc = 0; vc < n_chunks; ++vc) {
+              mma_commit(BAR(B_EMPTY + ring));
+              if (++ring == kStages) { ring = 0; ring_ph ^= 1; }
+            }
+            mma_commit(BAR(B_PVDONE));
+            return true;
+          }
           for (int vc = 0; vc < n_chunks; ++vc) {
             if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
             fence_proxy_async_smem();
