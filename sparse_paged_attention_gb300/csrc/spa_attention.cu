@@ -7,8 +7,9 @@
 //   gather warps (5..)   resolve columns through the block tables (FreeToken PR 633, "Changes":
 //                        per-column choice of window or compressed pool), then copy every K and V
 //                        row into shared memory, already in the 128-byte-swizzled operand layout,
-//                        through a 4-slot ring: bf16 rows by tensor-map gathers (four rows of 128
-//                        bytes per copy, eight warps issuing), e4m3 rows by 16-byte cp.async.
+//                        through a 4-slot ring: by tensor-map gathers (four rows of 128 bytes per
+//                        copy, six warps issuing in pairs) when CTAs take several items, by
+//                        16-byte cp.async (four warps) in CTAs of a single item (decode).
 //   MMA warp (4)         S^T[c][h] = K[c][:] . Q[h][:]    tcgen05, M = 128 columns, N = heads
 //                        O^T[d][h] += V[c][d] * P^T[c][h] tcgen05, M = 128 of head_dim, N = 64
 //                        both accumulate in TMEM (S^T double-buffered, O^T resident).
