@@ -17,6 +17,7 @@ float64 CPU oracle on the host cores instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import re
 import glob
 import hashlib
 import json
@@ -99,12 +100,18 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and blank space removed: a counter capture stays
+    valid across comment edits, and no longer once any code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_paged_attention_gb300", "csrc")
     for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
                     + glob.glob(os.path.join(csrc, "*.h"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+        with open(p, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(os.path.basename(p).encode() + text.encode())
     return h.hexdigest()[:16]
 
 
