@@ -38,6 +38,7 @@ HEADLINE = "decode_b1_r4"
 SUB_WORKLOADS = ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0", "prefill_s8192_r4",
                  "prefill_fp8_s4096_r4", "decode_b1_r128", "decode_b1_r0", "prefill_s2048_r4",
                  "prefill_s4096at28672_r4", "prefill_s8192_r128", "prefill_s8192_r0"]
+KV_WRITES = {"kv_write_fp8_t65536": True, "kv_write_t65536": False}   # name -> e4m3 pool
 FLUSH_BYTES = 512 << 20   # > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -336,6 +337,38 @@ def measure_workload(name, device, steps, warmup, flush, peaks):
     return d
 
 
+def measure_kv_write(name, device, steps, flush, peaks):
+    """The paged KV write of 65536 new tokens (head_dim 512, pages of 64) into a pool twice that
+    size: HBM-bound, bytes = 4·D read per token plus 2·D (e4m3 codes, and two fp32 scales) or
+    4·D (bf16) written."""
+    import numpy as np
+    import torch
+    import sparse_paged_attention_gb300 as spa
+    from workloads import kv_write_inputs
+    fp8 = KV_WRITES[name]
+    T, D, ps = 65536, 512, 64
+    inp = kv_write_inputs([np.arange(T)], D, ps, seed=3, specials=False)
+    nb = inp.num_blocks
+    kv = torch.zeros((nb, ps, 2, D), dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
+    ks = torch.zeros(nb * ps, dtype=torch.float32, device=device)
+    vs = torch.zeros_like(ks)
+    pool = spa.PagedPool(kv, inp.block_table.to(device), ks, vs)
+    k, v = inp.k.to(device), inp.v.to(device)
+    pos, sot = inp.positions.to(device), inp.seq_of_token.to(device)
+    fn = spa.sparse_attn_paged_kv_write_fp8 if fp8 else spa.sparse_attn_paged_kv_write
+    call = lambda: fn(k, v, pos, pool, seq_of_token=sot)
+    call()
+    if spa.sparse_attn_paged_check_errors():
+        raise RuntimeError(f"{name}: device error word")
+    times = time_device(call, steps, 3, flush)
+    us = 1e3 * statistics.mean(times)
+    nbytes = T * (4 * D + (2 * D + 8 if fp8 else 4 * D))
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
+            "calls": steps, "algorithmic_bytes": nbytes, "bound": "hbm", "achieved": round(gbs, 1),
+            "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def cpu_baseline(name, seconds):
     """The float64 oracle as it stands, on the host cores, in a fresh process."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
@@ -415,6 +448,11 @@ def run_gpu(args):
                     n = 50 if name.startswith("decode") else 10
                     sub[name] = measure_workload(name, device, n, 3, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - an unfinished path is reported, not fatal
+                    sub[name] = {"error": str(e)[:300]}
+            for name in KV_WRITES:
+                try:
+                    sub[name] = measure_kv_write(name, device, 50, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - reported, not fatal
                     sub[name] = {"error": str(e)[:300]}
         # keep the GPU busy long enough for the clock sampler to see it under load
         r = Runner(headline, device)

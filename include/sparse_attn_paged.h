@@ -156,6 +156,33 @@ int sparse_attn_paged_decode_noalloc(const void* q, const spa_pool_t* win, const
 int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* cmp,
                                       const spa_problem_t* prob, int32_t* cols, void* stream);
 
+/*
+ * Paged KV write: the step that fills the pools the attention reads.  Token t's K row k[t][:] and
+ * V row v[t][:] (bf16, one kv_head, head_dim D each; [T][D] row-major, 16-byte aligned) go to the
+ * pool slot of its position: row = block_table[b][x / page_size] * page_size + x % page_size
+ * with x = positions[t] and b = seq_of_token[t] (NULL: every token in sequence 0).  Slot row of
+ * pool.kv is [2][D]: K then V (the layout of the FreeToken PR 633 pools).  Rows of other slots are
+ * untouched.
+ *   - sparse_attn_paged_kv_write: bf16 pools, the rows are copied.
+ *   - sparse_attn_paged_kv_write_fp8: e4m3 pools (FreeToken clone PR 3, "Perf/kv fp8 read path":
+ *     one scale per token and kv_head, separately for K and V).  For each row x (fp32 values of the
+ *     bf16 inputs): scale = max|x| / 448 (IEEE fp32 division; 1 if the row is all zero), codes =
+ *     e4m3(x_i / scale), fp32 division then round to nearest even (the largest magnitude, 448,
+ *     cannot be exceeded by more than rounding and saturates there).  Scales go to
+ *     pool.k_scale / pool.v_scale [row].
+ * A token whose position is negative, whose page is past the block table's stride, whose block id
+ * is outside [0, num_blocks) or whose sequence id is outside [0, num_seqs) is skipped and sets
+ * SPA_ERR_INDEX in the device error word.  Two tokens writing one slot: the later write is not
+ * defined.  head_dim: a multiple of 64, at most 512.  Asynchronous on `stream`.
+ */
+int sparse_attn_paged_kv_write(const void* k, const void* v, int32_t num_tokens, int32_t head_dim,
+                               const int32_t* positions, const int32_t* seq_of_token,
+                               int32_t num_seqs, const spa_pool_t* pool, void* stream);
+int sparse_attn_paged_kv_write_fp8(const void* k, const void* v, int32_t num_tokens,
+                                   int32_t head_dim, const int32_t* positions,
+                                   const int32_t* seq_of_token, int32_t num_seqs,
+                                   const spa_pool_t* pool, void* stream);
+
 /* Synchronises `stream`, returns the device error word (an OR of SPA_ERR_INDEX and
  * SPA_ERR_TIMEOUT, 0 if clean) accumulated since the last check on the current device, and
  * clears it.  Returns SPA_ERR_CUDA if the synchronisation itself fails. */

@@ -18,7 +18,8 @@ What it follows (sources are the pages' titles and sections):
   max normal 448) and bfloat16 (the upper 16 bits of IEEE binary32).
 
 Parity status of each function is stated in its docstring.  Every function below is pinned by
-``tests/test_oracle_pins.py``.
+``tests/test_oracle_pins.py``; the paged KV write (``oracle.kv_write``: e4m3 encoding with round
+to nearest even, one scale per row, slot placement) by ``tests/test_oracle_kv_write.py``.
 """
 from .sparse_attention import (  # noqa: F401
     COL_POOL_SHIFT,
@@ -31,3 +32,4 @@ from .sparse_attention import (  # noqa: F401
     resolve_columns,
     sparse_paged_attention,
 )
+from . import kv_write  # noqa: F401

@@ -21,7 +21,8 @@ __all__ = [
     "PagedPool", "SpaError", "library_path", "load_library", "sparse_attn_paged_prefill",
     "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8",
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
-    "sparse_attn_paged_resolve_columns",
+    "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
+    "sparse_attn_paged_kv_write_fp8",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -90,6 +91,11 @@ def load_library():
     lib.sparse_attn_paged_decode_workspace_size.restype = ctypes.c_size_t
     lib.sparse_attn_paged_resolve_columns.argtypes = [PP, PP, PR, P, P]
     lib.sparse_attn_paged_resolve_columns.restype = ctypes.c_int
+    I32 = ctypes.c_int32
+    for name in ("sparse_attn_paged_kv_write", "sparse_attn_paged_kv_write_fp8"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, I32, I32, P, P, I32, PP, P]
+        f.restype = ctypes.c_int
     lib.sparse_attn_paged_check_errors.argtypes = [P]
     lib.sparse_attn_paged_check_errors.restype = ctypes.c_int
     lib.sparse_attn_paged_strerror.argtypes = [ctypes.c_int]
@@ -231,6 +237,36 @@ def sparse_attn_paged_decode_noalloc(q, win, cmp, topk_idx, positions, *, window
     if st != 0:
         raise SpaError(st, "sparse_attn_paged_decode_noalloc")
     return out
+
+
+def _kv_write(fp8, k, v, positions, pool, *, seq_of_token=None, num_seqs=None, stream=None):
+    lib = load_library()
+    for name, t in (("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 [num_tokens, head_dim] tensor")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    for name, t in (("positions", positions), ("seq_of_token", seq_of_token)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    T, D = int(k.shape[0]), int(k.shape[1])
+    B = int(pool.block_table.shape[0]) if num_seqs is None else int(num_seqs)
+    c = _pool_c(pool, fp8)
+    fn = lib.sparse_attn_paged_kv_write_fp8 if fp8 else lib.sparse_attn_paged_kv_write
+    st = fn(k.data_ptr(), v.data_ptr(), T, D, positions.data_ptr(), _ptr(seq_of_token), B,
+            ctypes.byref(c), _stream(stream))
+    if st != 0:
+        raise SpaError(st, fn.__name__)
+
+
+def sparse_attn_paged_kv_write(k, v, positions, pool, **kw):
+    """Copy the K and V rows of new tokens (bf16 [T, D]) into their slots of a bf16 pool."""
+    _kv_write(False, k, v, positions, pool, **kw)
+
+
+def sparse_attn_paged_kv_write_fp8(k, v, positions, pool, **kw):
+    """Quantise the K and V rows of new tokens to e4m3 (one scale per row) into an e4m3 pool."""
+    _kv_write(True, k, v, positions, pool, **kw)
 
 
 def sparse_attn_paged_resolve_columns(win, cmp, topk_idx, positions, *, window, ratio,

@@ -353,6 +353,42 @@ int decode_with_partials(const void* q, const spa_pool_t* win, const spa_pool_t*
 }
 }  // namespace spa
 
+namespace {
+int kv_write(const void* k, const void* v, int32_t T, int32_t D, const int32_t* positions,
+             const int32_t* seq_of_token, int32_t B, const spa_pool_t* pool, void* stream,
+             bool fp8) {
+  if (T < 0 || B < 1 || D < 1) return SPA_ERR_SHAPE;
+  if (D % 64 != 0 || D > 512) return SPA_ERR_UNSUPPORTED;
+  if (T == 0) return SPA_OK;
+  if (!k || !v || !positions) return SPA_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v)) return SPA_ERR_ALIGN;
+  const int st = check_pool(pool, fp8, D);
+  if (st) return st;
+  int dev = 0, sms = 0;
+  const int ds = current_device(&dev, &sms);
+  if (ds) return ds;
+  spa::KvWriteArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.k = static_cast<const uint8_t*>(k);
+  a.v = static_cast<const uint8_t*>(v);
+  a.kv = static_cast<uint8_t*>(const_cast<void*>(pool->kv));       // written by these calls
+  a.k_scale = const_cast<float*>(pool->k_scale);
+  a.v_scale = const_cast<float*>(pool->v_scale);
+  a.bt = pool->block_table;
+  a.positions = positions;
+  a.seq_of_token = seq_of_token;
+  a.num_blocks = pool->num_blocks;
+  a.T = T;
+  a.D = D;
+  a.B = B;
+  a.ps = pool->page_size;
+  a.bt_stride = pool->bt_stride;
+  const cudaError_t e = spa::launch_kv_write(a, fp8, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv write kernel launch");
+  return SPA_OK;
+}
+}  // namespace
+
 extern "C" {
 
 int sparse_attn_paged_prefill(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
@@ -407,13 +443,31 @@ int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* c
   return SPA_OK;
 }
 
+int sparse_attn_paged_kv_write(const void* k, const void* v, int32_t num_tokens, int32_t head_dim,
+                               const int32_t* positions, const int32_t* seq_of_token,
+                               int32_t num_seqs, const spa_pool_t* pool, void* stream) {
+  return kv_write(k, v, num_tokens, head_dim, positions, seq_of_token, num_seqs, pool, stream,
+                  false);
+}
+
+int sparse_attn_paged_kv_write_fp8(const void* k, const void* v, int32_t num_tokens,
+                                   int32_t head_dim, const int32_t* positions,
+                                   const int32_t* seq_of_token, int32_t num_seqs,
+                                   const spa_pool_t* pool, void* stream) {
+  return kv_write(k, v, num_tokens, head_dim, positions, seq_of_token, num_seqs, pool, stream,
+                  true);
+}
+
 int sparse_attn_paged_check_errors(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   int v = 0;
   e = spa::read_and_clear_error_word(&v);
   if (e != cudaSuccess) return cuda_fail(e, "device error word");
-  return v;
+  int w = 0;
+  e = spa::read_and_clear_kv_write_error_word(&w);
+  if (e != cudaSuccess) return cuda_fail(e, "device error word");
+  return v | w;
 }
 
 const char* sparse_attn_paged_strerror(int status) {

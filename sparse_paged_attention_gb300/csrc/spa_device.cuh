@@ -36,7 +36,8 @@ constexpr int kColPoolShift = 30;
 
 // Device error word: OR of SPA_ERR_INDEX / SPA_ERR_TIMEOUT.  Every translation unit that
 // includes this header has its own copy on every device that loads the library; the host reads
-// and clears them all in sparse_attn_paged_check_errors.
+// and clears the copies of the units whose kernels set it (spa_attention.cu, spa_kvwrite.cu) in
+// sparse_attn_paged_check_errors.
 static __device__ int g_spa_error;
 
 __device__ __forceinline__ void flag_error(int code) { atomicOr(&g_spa_error, code); }

@@ -53,6 +53,22 @@ int attn_max_active_clusters(int cluster, bool fp8);
 int merge_max_splits();
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_resolve_dump(const ResolveArgs& a, int32_t* cols, cudaStream_t stream);
+
+// Paged KV write (the step that fills the pools).
+struct KvWriteArgs {
+  const uint8_t* k;           // bf16 [T][D]
+  const uint8_t* v;           // bf16 [T][D]
+  uint8_t* kv;                // pool [num_blocks][page_size][2][D] (bf16 or e4m3)
+  float* k_scale;             // e4m3 pools: [num_blocks * page_size]
+  float* v_scale;
+  const int32_t* bt;          // [B][bt_stride]
+  const int32_t* positions;   // [T]
+  const int32_t* seq_of_token;  // [T] or NULL
+  long long num_blocks;
+  int T, D, B, ps, bt_stride;
+};
+cudaError_t launch_kv_write(const KvWriteArgs& a, bool fp8, cudaStream_t stream);
+cudaError_t read_and_clear_kv_write_error_word(int* value);
 cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)
 cudaError_t read_and_clear_error_word(int* value);
 

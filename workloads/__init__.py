@@ -311,3 +311,45 @@ def make(name: str, seed: int = 0) -> Workload:
         r = int(r)
         return build(name, seq_positions=[np.arange(0, int(S))], topk=topk_of[r], ratio=r, **big)
     raise KeyError(name)
+
+
+@dataclass
+class KvWriteInputs:
+    """New K/V rows of T tokens and the pages they go to (the paged KV write)."""
+    k: torch.Tensor              # bf16 [T, D]
+    v: torch.Tensor              # bf16 [T, D]
+    positions: torch.Tensor      # int32 [T]
+    seq_of_token: torch.Tensor   # int32 [T]
+    block_table: torch.Tensor    # int32 [B, stride]
+    num_blocks: int
+    page_size: int
+
+
+def kv_write_inputs(seq_positions: Sequence[np.ndarray], head_dim: int, page_size: int,
+                    seed: int = 0, oversize: int = 2, specials: bool = True) -> KvWriteInputs:
+    """Seeded inputs of a KV write: N(0,1) bf16 rows for tokens at the given positions of each
+    sequence, random pages from a pool `oversize` times larger than needed.  With `specials`, a few
+    rows are made awkward for the quantiser: all zeros, mixed signed zeros, one large element among
+    tiny ones (subnormal codes), and values at the half-way points between e4m3 codes."""
+    g = torch.Generator().manual_seed(seed)
+    pos = np.concatenate([np.asarray(p, dtype=np.int64) for p in seq_positions])
+    sid = np.concatenate([np.full(len(p), b, dtype=np.int64) for b, p in enumerate(seq_positions)])
+    pages = [int(np.max(p)) // page_size + 1 if len(p) else 1 for p in seq_positions]
+    num_blocks, table = _assign_pages(g, pages, oversize)
+    T = len(pos)
+    k = torch.randn(T, head_dim, generator=g)
+    v = torch.randn(T, head_dim, generator=g)
+    if specials and T >= 4:
+        k[0] = 0.0
+        v[0] = -0.0
+        k[1, ::2] = -0.0
+        k[1, 1::2] = 0.0
+        k[1, 0] = 3.0
+        k[2] = torch.randn(head_dim, generator=g) * 1e-4
+        k[2, 5] = 1000.0
+        # x = 448 * (m + 0.5) / 2^j / 448 * amax -> exact half-way points once divided by the scale
+        v[3] = torch.tensor([((8 + (i % 8)) + 0.5) * 2.0 ** (-(i % 6)) for i in range(head_dim)])
+        v[3, 0] = 448.0
+    return KvWriteInputs(k.to(torch.bfloat16), v.to(torch.bfloat16),
+                         torch.from_numpy(pos.astype(np.int32)),
+                         torch.from_numpy(sid.astype(np.int32)), table, num_blocks, page_size)
