@@ -39,6 +39,8 @@ SUB_WORKLOADS = ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0", "prefill_s819
                  "prefill_fp8_s4096_r4", "decode_b1_r128", "decode_b1_r0", "prefill_s2048_r4",
                  "prefill_s4096at28672_r4", "prefill_s8192_r128", "prefill_s8192_r0"]
 KV_WRITES = {"kv_write_fp8_t65536": True, "kv_write_t65536": False}   # name -> e4m3 pool
+GATED_POOLS = {"gated_pool_b%d_r%d_d%d" % s: s for s in
+               [(b, r, d) for b in (1, 8) for r in (8, 128) for d in (128, 512)]}
 FLUSH_BYTES = 512 << 20   # > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -369,6 +371,29 @@ def measure_kv_write(name, device, steps, flush, peaks):
             "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+def measure_gated_pool(name, device, steps, flush, peaks):
+    """The compressor's gated pool at one of the pages' shapes (B entries of R rows, D channels,
+    fp32 output): HBM- and latency-bound, bytes = 8·B·R·D read (kv and gates) + 4·B·D written."""
+    import torch
+    import sparse_paged_attention_gb300 as spa
+    from workloads import gated_pool_inputs
+    B, R, D = GATED_POOLS[name]
+    _, kv, _, gate = gated_pool_inputs(B, R, D, seed=4)
+    kv, gate = kv.to(device), gate.to(device)
+    out = torch.empty((B, D), dtype=torch.float32, device=device)
+    call = lambda: spa.sparse_attn_gated_pool(kv, gate, out)
+    call()
+    times = time_device(call, steps, 3, flush)
+    us = 1e3 * statistics.mean(times)
+    warm = 1e3 * time_graph(call)
+    nbytes = 8 * B * R * D + 4 * B * D
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
+            "warm_l2_graph_us": round(warm, 3), "calls": steps, "algorithmic_bytes": nbytes,
+            "bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def cpu_baseline(name, seconds):
     """The float64 oracle as it stands, on the host cores, in a fresh process."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
@@ -452,6 +477,11 @@ def run_gpu(args):
             for name in KV_WRITES:
                 try:
                     sub[name] = measure_kv_write(name, device, 50, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - reported, not fatal
+                    sub[name] = {"error": str(e)[:300]}
+            for name in GATED_POOLS:
+                try:
+                    sub[name] = measure_gated_pool(name, device, 50, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
                     sub[name] = {"error": str(e)[:300]}
         # keep the GPU busy long enough for the clock sampler to see it under load

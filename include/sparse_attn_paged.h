@@ -183,6 +183,35 @@ int sparse_attn_paged_kv_write_fp8(const void* k, const void* v, int32_t num_tok
                                    const int32_t* seq_of_token, int32_t num_seqs,
                                    const spa_pool_t* pool, void* stream);
 
+/*
+ * Gated pool of the KV compressor (FreeToken PR 633, call paths: the DeepSeek-V4 compressor's
+ * decode step folds R buffered rows into one compressed entry; "Changes": a maximum over R, then a
+ * weighted pass).  For every entry b and channel d, a softmax of the gates over the R rows weighs
+ * the kv rows:
+ *     out[b][d] = sum_r exp(gate[b][r][d] - M) * kv[b][r][d] / sum_r exp(gate[b][r][d] - M),
+ *     M = max_r gate[b][r][d].
+ * (The page prints no formula; this per-channel softmax is the reading taken.)
+ *   kv, gate:  fp32 device arrays [batch][rows][dim], innermost stride 1, other strides in
+ *              elements (>= 0; strided views allowed); 4-byte aligned.  Rows that start 16-byte
+ *              aligned (base and strides multiples of 4 elements, dim % 4 == 0) are read with
+ *              16-byte loads, others with 4-byte loads: same result.
+ *   out:       device array [batch][dim] of out_dtype (SPA_DTYPE_F32 or SPA_DTYPE_BF16, rounded to
+ *              nearest even), innermost stride 1, batch stride out_stride_b elements; aligned to
+ *              its element size.  Must not overlap kv or gate.
+ *   rows == 0 writes zeros.  batch == 0 or dim == 0 does nothing.  Arithmetic is fp32 with one
+ *   online maximum per channel (the rows are read once).  Gates of +-inf or NaN give what the
+ *   formula gives in IEEE arithmetic (NaN where it is undefined).
+ * Returns SPA_ERR_SHAPE for negative sizes or strides, SPA_ERR_NULL, SPA_ERR_ALIGN,
+ * SPA_ERR_UNSUPPORTED for an unknown out_dtype, SPA_ERR_CUDA if the launch fails.  Asynchronous on
+ * `stream`; allocates nothing.
+ */
+#define SPA_DTYPE_F32 0
+#define SPA_DTYPE_BF16 1
+int sparse_attn_gated_pool(const float* kv, const float* gate, int32_t batch, int32_t rows,
+                           int32_t dim, int64_t kv_stride_b, int64_t kv_stride_r,
+                           int64_t gate_stride_b, int64_t gate_stride_r, void* out,
+                           int32_t out_dtype, int64_t out_stride_b, void* stream);
+
 /* Synchronises `stream`, returns the device error word (an OR of SPA_ERR_INDEX and
  * SPA_ERR_TIMEOUT, 0 if clean) accumulated since the last check on the current device, and
  * clears it.  Returns SPA_ERR_CUDA if the synchronisation itself fails. */

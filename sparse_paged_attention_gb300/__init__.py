@@ -22,7 +22,7 @@ __all__ = [
     "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8",
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
     "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
-    "sparse_attn_paged_kv_write_fp8",
+    "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -96,6 +96,9 @@ def load_library():
         f = getattr(lib, name)
         f.argtypes = [P, P, I32, I32, P, P, I32, PP, P]
         f.restype = ctypes.c_int
+    I64 = ctypes.c_int64
+    lib.sparse_attn_gated_pool.argtypes = [P, P, I32, I32, I32, I64, I64, I64, I64, P, I32, I64, P]
+    lib.sparse_attn_gated_pool.restype = ctypes.c_int
     lib.sparse_attn_paged_check_errors.argtypes = [P]
     lib.sparse_attn_paged_check_errors.restype = ctypes.c_int
     lib.sparse_attn_paged_strerror.argtypes = [ctypes.c_int]
@@ -267,6 +270,34 @@ def sparse_attn_paged_kv_write(k, v, positions, pool, **kw):
 def sparse_attn_paged_kv_write_fp8(k, v, positions, pool, **kw):
     """Quantise the K and V rows of new tokens to e4m3 (one scale per row) into an e4m3 pool."""
     _kv_write(True, k, v, positions, pool, **kw)
+
+
+def sparse_attn_gated_pool(kv, gate, out=None, *, out_dtype=torch.float32, stream=None):
+    """The compressor's gated pool: ``out[b, d] = sum_r softmax_r(gate[b, :, d]) * kv[b, r, d]``.
+
+    ``kv`` and ``gate``: fp32 CUDA tensors [B, R, D] with a contiguous last dimension (strided
+    views otherwise allowed).  ``out``: [B, D] fp32 or bf16 with a contiguous last dimension, made
+    here when not given (of ``out_dtype``).
+    """
+    lib = load_library()
+    for name, t in (("kv", kv), ("gate", gate)):
+        if t.dtype != torch.float32 or t.dim() != 3 or (t.shape[2] > 1 and t.stride(2) != 1):
+            raise ValueError(f"{name} must be an fp32 [B, R, D] tensor with unit last stride")
+    if kv.shape != gate.shape:
+        raise ValueError("kv and gate must have the same shape")
+    B, R, D = (int(x) for x in kv.shape)
+    if out is None:
+        out = torch.empty((B, D), dtype=out_dtype, device=kv.device)
+    if out.dtype not in (torch.float32, torch.bfloat16) or tuple(out.shape) != (B, D) or \
+            (D > 1 and out.stride(1) != 1):
+        raise ValueError("out must be an fp32 or bf16 [B, D] tensor with unit last stride")
+    dt = 1 if out.dtype == torch.bfloat16 else 0
+    st = lib.sparse_attn_gated_pool(kv.data_ptr(), gate.data_ptr(), B, R, D, kv.stride(0),
+                                    kv.stride(1), gate.stride(0), gate.stride(1), out.data_ptr(),
+                                    dt, out.stride(0), _stream(stream))
+    if st != 0:
+        raise SpaError(st, "sparse_attn_gated_pool")
+    return out
 
 
 def sparse_attn_paged_resolve_columns(win, cmp, topk_idx, positions, *, window, ratio,

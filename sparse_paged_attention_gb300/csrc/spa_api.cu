@@ -443,6 +443,42 @@ int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* c
   return SPA_OK;
 }
 
+int sparse_attn_gated_pool(const float* kv, const float* gate, int32_t batch, int32_t rows,
+                           int32_t dim, int64_t kv_stride_b, int64_t kv_stride_r,
+                           int64_t gate_stride_b, int64_t gate_stride_r, void* out,
+                           int32_t out_dtype, int64_t out_stride_b, void* stream) {
+  if (batch < 0 || rows < 0 || dim < 0 || kv_stride_b < 0 || kv_stride_r < 0 ||
+      gate_stride_b < 0 || gate_stride_r < 0 || out_stride_b < 0)
+    return SPA_ERR_SHAPE;
+  if (out_dtype != SPA_DTYPE_F32 && out_dtype != SPA_DTYPE_BF16) return SPA_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SPA_OK;
+  if (!out || (rows > 0 && (!kv || !gate))) return SPA_ERR_NULL;
+  const uintptr_t out_align = out_dtype == SPA_DTYPE_BF16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(kv) & 3u) || (reinterpret_cast<uintptr_t>(gate) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out) & (out_align - 1)))
+    return SPA_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  const int ds = current_device(&dev, &sms);
+  if (ds) return ds;
+  spa::GatedPoolArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.kv = kv;
+  g.gate = gate;
+  g.out = out;
+  g.kv_sb = kv_stride_b;
+  g.kv_sr = kv_stride_r;
+  g.gate_sb = gate_stride_b;
+  g.gate_sr = gate_stride_r;
+  g.out_sb = out_stride_b;
+  g.B = batch;
+  g.R = rows;
+  g.D = dim;
+  g.out_bf16 = out_dtype == SPA_DTYPE_BF16;
+  const cudaError_t e = spa::launch_gated_pool(g, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gated pool kernel launch");
+  return SPA_OK;
+}
+
 int sparse_attn_paged_kv_write(const void* k, const void* v, int32_t num_tokens, int32_t head_dim,
                                const int32_t* positions, const int32_t* seq_of_token,
                                int32_t num_seqs, const spa_pool_t* pool, void* stream) {

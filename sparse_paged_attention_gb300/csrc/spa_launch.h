@@ -69,6 +69,24 @@ struct KvWriteArgs {
 };
 cudaError_t launch_kv_write(const KvWriteArgs& a, bool fp8, cudaStream_t stream);
 cudaError_t read_and_clear_kv_write_error_word(int* value);
+// Gated pool of the KV compressor (R rows -> one entry per channel).
+constexpr int kGatedPoolMaxWarps = 16;
+struct GatedPoolArgs {
+  const float* kv;             // [B][R][D] fp32, element strides kv_sb, kv_sr, 1
+  const float* gate;           // [B][R][D] fp32, element strides gate_sb, gate_sr, 1
+  void* out;                   // [B][D] fp32 or bf16, element stride out_sb, 1
+  long long kv_sb, kv_sr, gate_sb, gate_sr, out_sb;
+  int B, R, D;
+  int out_bf16;
+};
+// 4 when every row of kv and gate starts 16-byte aligned (float4 loads), else 1
+inline int gated_pool_vector_width(const GatedPoolArgs& g) {
+  const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool rows4 = (g.R <= 1 || (g.kv_sr % 4 == 0 && g.gate_sr % 4 == 0)) &&
+                     (g.B <= 1 || (g.kv_sb % 4 == 0 && g.gate_sb % 4 == 0));
+  return (g.D % 4 == 0 && a16(g.kv) && a16(g.gate) && rows4) ? 4 : 1;
+}
+cudaError_t launch_gated_pool(const GatedPoolArgs& g, cudaStream_t stream);
 cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)
 cudaError_t read_and_clear_error_word(int* value);
 

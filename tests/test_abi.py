@@ -26,7 +26,7 @@ def declared_functions():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names |= set(re.findall(r"\b(sparse_attn_paged_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(sparse_attn_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -34,7 +34,9 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("sparse_attn_paged_prefill", "sparse_attn_paged_decode",
                  "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode_fp8",
-                 "sparse_attn_paged_resolve_columns", "sparse_attn_paged_check_errors"):
+                 "sparse_attn_paged_resolve_columns", "sparse_attn_paged_check_errors",
+                 "sparse_attn_paged_kv_write", "sparse_attn_paged_kv_write_fp8",
+                 "sparse_attn_gated_pool"):
         assert must in names
 
 
@@ -48,6 +50,16 @@ def test_strerror_and_version(lib):
                        (4, "SPA_ERR_UNSUPPORTED"), (8, "SPA_ERR_INDEX"), (16, "SPA_ERR_TIMEOUT")]:
         assert spa.sparse_attn_paged_strerror(code).startswith(name)
     assert b"sm_103a" in lib.sparse_attn_paged_version()
+
+
+@pytest.fixture
+def no_device():
+    """The validation tests below hand made-up device addresses to the entry points.  A call that
+    passes host validation would launch a kernel on them, so they run only where no GPU is
+    visible (the library then stops at its device query)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("made-up device addresses: host validation is tested without a GPU")
 
 
 def _args(D=512, W=128, K=512, ratio=4, T=1, kv=0x1000, q=0x2000, out=0x3000):
@@ -64,7 +76,7 @@ def _prefill(lib, pool, cpool, prob, q, out):
                                          None)
 
 
-def test_host_validation(lib):
+def test_host_validation(lib, no_device):
     S = spa.SPA_STATUS
     pool, cpool, prob, q, out = _args()
     assert _prefill(lib, pool, cpool, None, q, out) == S["SPA_ERR_NULL"]
@@ -88,7 +100,25 @@ def test_host_validation(lib):
     # fp8 pools need their scales
     assert lib.sparse_attn_paged_prefill_fp8(q, ctypes.byref(pool), ctypes.byref(cpool),
                                              ctypes.byref(prob), out, None) == S["SPA_ERR_NULL"]
-    # decode: workspace checks come before any launch
+    # decode: with no device visible the call stops at the device query
     assert lib.sparse_attn_paged_decode(q, ctypes.byref(pool), ctypes.byref(cpool),
                                         ctypes.byref(prob), out, None, 0, None) in (
         S["SPA_ERR_NULL"], S["SPA_ERR_CUDA"])
+
+
+def test_gated_pool_host_validation(lib, no_device):
+    S = spa.SPA_STATUS
+    f = lib.sparse_attn_gated_pool
+    kv, g, out = 0x10000, 0x20000, 0x30000
+
+    def call(kv=kv, g=g, B=8, R=128, D=512, sb=65536, sr=512, out=out, dt=0, osb=512):
+        return f(kv, g, B, R, D, sb, sr, sb, sr, out, dt, osb, None)
+    assert call(B=-1) == S["SPA_ERR_SHAPE"]
+    assert call(R=-1) == S["SPA_ERR_SHAPE"]
+    assert call(sr=-4) == S["SPA_ERR_SHAPE"]
+    assert call(osb=-1) == S["SPA_ERR_SHAPE"]
+    assert call(dt=2) == S["SPA_ERR_UNSUPPORTED"]
+    assert call(B=0) == S["SPA_OK"] and call(D=0) == S["SPA_OK"]     # nothing to do
+    assert call(kv=None) == S["SPA_ERR_NULL"] and call(out=None) == S["SPA_ERR_NULL"]
+    assert call(kv=kv + 2) == S["SPA_ERR_ALIGN"] and call(g=g + 1) == S["SPA_ERR_ALIGN"]
+    assert call(out=out + 2) == S["SPA_ERR_ALIGN"]                   # fp32 out: 4-byte aligned

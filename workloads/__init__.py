@@ -353,3 +353,37 @@ def kv_write_inputs(seq_positions: Sequence[np.ndarray], head_dim: int, page_siz
     return KvWriteInputs(k.to(torch.bfloat16), v.to(torch.bfloat16),
                          torch.from_numpy(pos.astype(np.int32)),
                          torch.from_numpy(sid.astype(np.int32)), table, num_blocks, page_size)
+
+
+# gated-pool shapes timed on the pages (FreeToken PR 633, "Kernel time": B, R, D)
+GATED_POOL_SHAPES = [(b, r, d) for b in (1, 8) for r in (8, 128) for d in (128, 512)]
+
+
+def gated_pool_inputs(B: int, R: int, D: int, seed: int = 0, gate_std: float = 2.0,
+                      view: str = "dense"):
+    """Seeded gated-pool inputs: kv ~ N(0,1) and gates ~ N(0, gate_std^2), fp32 [B, R, D].
+
+    ``view`` makes strided views of larger buffers, as a compressor's state slices would be:
+    "dense" (contiguous), "row_pad" (rows 8 floats apart more than D, i.e. a [B, R, D + 8] buffer
+    cut to D), "every_other_row" (a [B, 2R, D] buffer, rows 0, 2, 4, ...), "odd_offset" (the view
+    starts one float into its buffer, so rows are 4-byte but not 16-byte aligned).
+    """
+    g = torch.Generator().manual_seed(seed)
+
+    def one(std):
+        if view == "dense":
+            t = torch.randn(B, R, D, generator=g) * std
+            return t, t
+        if view == "row_pad":
+            buf = torch.randn(B, R, D + 8, generator=g) * std
+            return buf, buf[:, :, :D]
+        if view == "every_other_row":
+            buf = torch.randn(B, 2 * R, D, generator=g) * std
+            return buf, buf[:, ::2, :]
+        if view == "odd_offset":
+            buf = torch.randn(B * R * D + 1, generator=g) * std
+            return buf, buf[1:].view(B, R, D)
+        raise ValueError(view)
+    kv_buf, kv = one(1.0)
+    gate_buf, gate = one(gate_std)
+    return kv_buf, kv, gate_buf, gate
