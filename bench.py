@@ -5,9 +5,11 @@ Headline: one decode call of the B=1 workload at position 32767 (64 heads, head_
 top-k 512 of 8192 compressed entries, ratio 4, page size 64; the shape of the FreeToken PR 633
 "Kernel time" table), in microseconds per call, L2 flushed between calls.  The same JSON line
 carries the other workloads of the table (decode B=8 at ratios 128/4/0, prefill S=8192, the e4m3
-prefill chunk) with their achieved GB/s or TFLOP/s against the measured GB300 peaks.
+prefill chunk), the paged KV write and the compressor's gated pool at the same page's shapes, with
+their achieved GB/s or TFLOP/s against the measured GB300 peaks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME] [--no-sub | --sub NAME,...] [--no-cpu-baseline]
 
 For N > 1 (torchrun, one rank per GPU) every rank runs the same workload on its own GPU (the
 problem shards into independent queries/sequences; there is no data-path collective): the
@@ -465,21 +467,23 @@ def run_gpu(args):
         work = algorithmic_work(r.w)
         del r
         sub = {}
+        only = None if args.sub is None else set(args.sub.split(","))
+        keep = lambda name: only is None or name in only
         if not args.no_sub:
             for name in SUB_WORKLOADS:
-                if name == headline:
+                if name == headline or not keep(name):
                     continue
                 try:
                     n = 50 if name.startswith("decode") else 10
                     sub[name] = measure_workload(name, device, n, 3, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - an unfinished path is reported, not fatal
                     sub[name] = {"error": str(e)[:300]}
-            for name in KV_WRITES:
+            for name in filter(keep, KV_WRITES):
                 try:
                     sub[name] = measure_kv_write(name, device, 50, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
                     sub[name] = {"error": str(e)[:300]}
-            for name in GATED_POOLS:
+            for name in filter(keep, GATED_POOLS):
                 try:
                     sub[name] = measure_gated_pool(name, device, 50, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
@@ -591,11 +595,18 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE,
                     help="headline workload (default: decode B=1, ratio 4); see workloads.make")
     ap.add_argument("--no-sub", action="store_true", help="headline workload only")
+    ap.add_argument("--sub", default=None,
+                    help="comma-separated names: measure only these of the other workloads "
+                         "(attention workloads, kv_write_*, gated_pool_*)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.sub is not None:
+        unknown = set(args.sub.split(",")) - set(SUB_WORKLOADS) - set(KV_WRITES) - set(GATED_POOLS)
+        if unknown:
+            ap.error(f"unknown --sub workload(s): {sorted(unknown)}")
     if args.impl == "reference":
         run_reference(args)
     else:

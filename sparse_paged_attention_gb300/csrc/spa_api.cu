@@ -474,7 +474,7 @@ int sparse_attn_gated_pool(const float* kv, const float* gate, int32_t batch, in
   g.R = rows;
   g.D = dim;
   g.out_bf16 = out_dtype == SPA_DTYPE_BF16;
-  const cudaError_t e = spa::launch_gated_pool(g, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = spa::launch_gated_pool(g, sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gated pool kernel launch");
   return SPA_OK;
 }

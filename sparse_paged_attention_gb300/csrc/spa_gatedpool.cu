@@ -6,11 +6,12 @@
 //
 // The work is a pure stream of 8·R·D bytes per entry with no reuse, so HBM (and, at the small
 // shapes the decode step runs, launch latency) bounds it.  One CTA takes 32·VEC channels of one
-// entry; its warps split the R rows (row r goes to warp r mod nw), each lane keeping an online
-// maximum, denominator and weighted sum for VEC adjacent channels over a one-pass read (no second
-// read of the rows for the maximum).  Rows are loaded eight at a time before any arithmetic, so
-// that a lane has 16 loads in flight.  The warps' partial states then merge through shared memory
-// by the same rescaling rule, and one thread per channel writes the result.
+// entry; its nw = ceil(R / 8) warps (at most 16) split the R rows, row r going to warp r mod nw, so
+// that a warp holds about eight rows.  Each lane keeps an online maximum, denominator and weighted
+// sum for VEC adjacent channels over a one-pass read (no second read of the rows for the maximum),
+// loading a batch of eight rows (16 loads) before any arithmetic.  With one warp the lane writes
+// its channels directly; otherwise the warps' states meet in shared memory and 16 lanes per channel
+// merge them by the same rescaling rule in a shuffle tree.
 #include <cuda_bf16.h>
 
 #include "spa_launch.h"
@@ -31,6 +32,13 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float& a, float 
   l = l * c1 + l2 * c2;
   a = a * c1 + a2 * c2;
   m = mn;
+}
+
+__device__ __forceinline__ void store_out(const GatedPoolArgs& g, long long b, int d, float o) {
+  if (g.out_bf16)
+    reinterpret_cast<__nv_bfloat16*>(g.out)[b * g.out_sb + d] = __float2bfloat16_rn(o);
+  else
+    reinterpret_cast<float*>(g.out)[b * g.out_sb + d] = o;
 }
 
 template <int VEC>
@@ -91,6 +99,13 @@ __global__ void __launch_bounds__(kGatedPoolMaxWarps * 32)
     }
   }
 
+  if (nw == 1) {  // this lane saw every row of its channels
+    if (live) {
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) store_out(g, b, d + v, g.R == 0 ? 0.f : acc[v] / l[v]);
+    }
+    return;
+  }
 #pragma unroll
   for (int v = 0; v < VEC; ++v) {
     s_m[warp][lane * VEC + v] = m[v];
@@ -98,31 +113,37 @@ __global__ void __launch_bounds__(kGatedPoolMaxWarps * 32)
     s_a[warp][lane * VEC + v] = acc[v];
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < CH; c += blockDim.x) {
-    const int dc = c0 + c;
-    if (dc >= g.D) break;
-    float mm = s_m[0][c], ll = s_l[0][c], aa = s_a[0][c];
-    for (int w = 1; w < nw; ++w) merge_state(mm, ll, aa, s_m[w][c], s_l[w][c], s_a[w][c]);
-    const float o = g.R == 0 ? 0.f : aa / ll;
-    if (g.out_bf16)
-      reinterpret_cast<__nv_bfloat16*>(g.out)[b * g.out_sb + dc] = __float2bfloat16_rn(o);
-    else
-      reinterpret_cast<float*>(g.out)[b * g.out_sb + dc] = o;
+  // lanes 0-15 of a warp merge one channel, lanes 16-31 the next; lane (tid & 15) brings the state
+  // of warp (tid & 15).  CH and the stride 2·nw are even, so both halves of a warp run the same
+  // trips and the full-mask shuffles are warp-uniform.
+  const int sub = threadIdx.x & 15;
+  for (int c = threadIdx.x >> 4; c < CH; c += blockDim.x >> 4) {
+    float mm = -INFINITY, ll = 0.f, aa = 0.f;
+    if (sub < nw) mm = s_m[sub][c], ll = s_l[sub][c], aa = s_a[sub][c];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
+      const float a2 = __shfl_xor_sync(0xffffffffu, aa, o);
+      merge_state(mm, ll, aa, m2, l2, a2);
+    }
+    if (sub == 0 && c0 + c < g.D) store_out(g, b, c0 + c, aa / ll);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gated_pool(const GatedPoolArgs& g, cudaStream_t stream) {
+cudaError_t launch_gated_pool(const GatedPoolArgs& g, int num_sms, cudaStream_t stream) {
   if (g.B == 0 || g.D == 0) return cudaSuccess;
-  const int vec = gated_pool_vector_width(g);
+  // 16-byte loads only when they still leave a CTA for every SM: at the decode step's sizes the
+  // narrower CTAs spread the rows over more SMs, which matters more than the load width
+  int vec = gated_pool_vector_width(g);
+  if (vec == 4 && (long long)g.B * ((g.D + 127) / 128) < num_sms) vec = 1;
   const long long chunks = (g.D + 32LL * vec - 1) / (32LL * vec);
   const long long blocks = (long long)g.B * chunks;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  // warps split the rows; a CTA needs at least VEC warps for its merge to cover 32·VEC channels
-  // in one pass (it loops otherwise), and never more than the shared state holds
-  int nw = g.R < 1 ? 1 : (g.R < kGatedPoolMaxWarps ? g.R : kGatedPoolMaxWarps);
-  if (nw < vec) nw = vec;
+  int nw = (g.R + kRowsPerBatch - 1) / kRowsPerBatch;  // about one batch of rows per warp
+  nw = nw < 1 ? 1 : (nw > kGatedPoolMaxWarps ? kGatedPoolMaxWarps : nw);
   if (vec == 4)
     gated_pool_kernel<4><<<(unsigned)blocks, nw * 32, 0, stream>>>(g);
   else

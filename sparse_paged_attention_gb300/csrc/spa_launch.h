@@ -79,14 +79,14 @@ struct GatedPoolArgs {
   int B, R, D;
   int out_bf16;
 };
-// 4 when every row of kv and gate starts 16-byte aligned (float4 loads), else 1
+// 4 when every row of kv and gate starts 16-byte aligned (float4 loads possible), else 1
 inline int gated_pool_vector_width(const GatedPoolArgs& g) {
   const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool rows4 = (g.R <= 1 || (g.kv_sr % 4 == 0 && g.gate_sr % 4 == 0)) &&
                      (g.B <= 1 || (g.kv_sb % 4 == 0 && g.gate_sb % 4 == 0));
   return (g.D % 4 == 0 && a16(g.kv) && a16(g.gate) && rows4) ? 4 : 1;
 }
-cudaError_t launch_gated_pool(const GatedPoolArgs& g, cudaStream_t stream);
+cudaError_t launch_gated_pool(const GatedPoolArgs& g, int num_sms, cudaStream_t stream);
 cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic shared memory)
 cudaError_t read_and_clear_error_word(int* value);
 

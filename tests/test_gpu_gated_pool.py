@@ -98,3 +98,10 @@ def test_output_row_stride_leaves_the_gaps():
     assert (got[:, 96:] == -3.0).all()
     ref = ogp.gated_pool(kv.numpy(), gate.numpy())
     assert np.abs(got[:, :96] - ref).max() <= 80 * 2.0 ** -24 * np.abs(kv.numpy()).max()
+
+
+@pytest.mark.parametrize("B,R,D,view", [(160, 20, 512, "dense"), (200, 33, 128, "row_pad"),
+                                        (156, 1, 256, "every_other_row")])
+def test_wide_batches(B, R, D, view):
+    """Enough CTAs for one per SM at 128 channels each: the 16-byte load path."""
+    _check(B, R, D, torch.float32, view=view, seed=B + R)
