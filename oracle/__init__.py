@@ -21,7 +21,9 @@ Parity status of each function is stated in its docstring.  Every function below
 ``tests/test_oracle_pins.py``; the paged KV write (``oracle.kv_write``: e4m3 encoding with round
 to nearest even, one scale per row, slot placement) by ``tests/test_oracle_kv_write.py``; the
 compressor's gated pool (``oracle.gated_pool``: a per-channel softmax over R rows weighting the kv
-rows, a stated reading) by ``tests/test_oracle_gated_pool.py``.
+rows, a stated reading) by ``tests/test_oracle_gated_pool.py``; the indexer logits over packed fp4
+key rows (``oracle.indexer``: OCP E2M1/E8M0 decoding, a stated logit reading) by
+``tests/test_oracle_indexer.py``.
 """
 from .sparse_attention import (  # noqa: F401
     COL_POOL_SHIFT,
@@ -34,4 +36,4 @@ from .sparse_attention import (  # noqa: F401
     resolve_columns,
     sparse_paged_attention,
 )
-from . import gated_pool, kv_write  # noqa: F401
+from . import gated_pool, indexer, kv_write  # noqa: F401

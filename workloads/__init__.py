@@ -387,3 +387,84 @@ def gated_pool_inputs(B: int, R: int, D: int, seed: int = 0, gate_std: float = 2
     kv_buf, kv = one(1.0)
     gate_buf, gate = one(gate_std)
     return kv_buf, kv, gate_buf, gate
+
+
+# ----------------------------------------------------------------------------------------------
+# indexer inputs (FreeToken PR 634: 32 index heads, index head_dim 128, fp4_e8m0_b32 key rows)
+# ----------------------------------------------------------------------------------------------
+INDEX_ROW_WORDS = 17
+NAN_SCALES_WORD = -1       # 0xFFFFFFFF: all four ue8m0 scale bytes NaN (poison for stray reads)
+
+
+@dataclass
+class IndexerInputs:
+    q: torch.Tensor             # bf16 [T, H, 128]
+    weights: torch.Tensor       # fp32 [T, H]
+    key_pool: torch.Tensor      # int32 [num_blocks, page_size, 17]
+    block_table: torch.Tensor   # int32 [B, stride]
+    positions: torch.Tensor     # int32 [T]
+    seq_of_token: torch.Tensor  # int32 [T]
+    ratio: int
+    num_cols: int
+    cand: Optional[torch.Tensor] = None   # int32 [T, num_cols] (candidate mode)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.block_table.shape[0])
+
+    def seq_ids(self) -> np.ndarray:
+        return self.seq_of_token.numpy().astype(np.int64)
+
+
+def indexer_inputs(seq_positions: Sequence[np.ndarray], ratio: int, *, num_heads: int = 32,
+                   page_size: int = 64, seed: int = 0, num_cols: Optional[int] = None,
+                   cand_count: Optional[int] = None, cand_fill: str = "tail",
+                   scale_exps=(121, 127), oversize: int = 2) -> IndexerInputs:
+    """Seeded indexer inputs.
+
+    Queries ~ N(0,1) in bf16, weights ~ N(0,1)/sqrt(H) in fp32.  Key rows of every compressed entry
+    each sequence has (``(max position + 1) // ratio``): uniformly random e2m1 nibbles and ue8m0
+    scale bytes drawn from ``scale_exps`` (inclusive), in random pages of a pool ``oversize`` times
+    larger; spare rows carry NaN scales.  Full mode: ``num_cols`` defaults to the largest entry
+    count.  Candidate mode (``cand_count``): per query a random choice of its causal entries,
+    padded with -1 at the tail ("tail") or with -1 and non-causal entries scattered ("anywhere").
+    """
+    g = torch.Generator().manual_seed(seed)
+    pos = np.concatenate([np.asarray(p, dtype=np.int64) for p in seq_positions])
+    sid = np.concatenate([np.full(len(p), b, dtype=np.int64) for b, p in enumerate(seq_positions)])
+    T = len(pos)
+    entries = [max(0, (int(np.max(p)) + 1) // ratio) if len(p) else 0 for p in seq_positions]
+    pages = [max(1, -(-e // page_size)) for e in entries]
+    num_blocks, table = _assign_pages(g, pages, oversize)
+    words = torch.randint(-(1 << 31), (1 << 31) - 1, (num_blocks * page_size, INDEX_ROW_WORDS),
+                          generator=g, dtype=torch.int64)
+    lo, hi = scale_exps
+    sc = torch.randint(lo, hi + 1, (num_blocks * page_size, 4), generator=g, dtype=torch.int64)
+    words[:, 16] = sc[:, 0] | (sc[:, 1] << 8) | (sc[:, 2] << 16) | (sc[:, 3] << 24)
+    words = ((words + (1 << 31)) % (1 << 32) - (1 << 31)).to(torch.int32)
+    used = torch.zeros(num_blocks, dtype=torch.bool)
+    used[table[table >= 0].long()] = True
+    rows_used = used.repeat_interleave(page_size)
+    words[~rows_used, 16] = NAN_SCALES_WORD
+    key_pool = words.view(num_blocks, page_size, INDEX_ROW_WORDS)
+    q = torch.randn(T, num_heads, 128, generator=g).to(torch.bfloat16)
+    weights = torch.randn(T, num_heads, generator=g) / float(np.sqrt(num_heads))
+    cand = None
+    if cand_count is None:
+        ncols = max(entries) if num_cols is None else num_cols
+    else:
+        ncols = cand_count
+        cand = torch.full((T, cand_count), -1, dtype=torch.int32)
+        for t in range(T):
+            valid = (int(pos[t]) + 1) // ratio
+            k = min(valid, cand_count)
+            pick = torch.randperm(valid, generator=g)[:k].to(torch.int32) if valid else \
+                torch.empty(0, dtype=torch.int32)
+            cand[t, :k] = pick
+            if cand_fill == "anywhere" and cand_count >= 4:
+                slots = torch.randperm(cand_count, generator=g)[:max(1, cand_count // 8)]
+                cand[t, slots[0::2]] = -1
+                cand[t, slots[1::2]] = int(pos[t]) // ratio + 1     # one entry past causality
+    return IndexerInputs(q, weights, key_pool, table,
+                         torch.from_numpy(pos.astype(np.int32)),
+                         torch.from_numpy(sid.astype(np.int32)), ratio, ncols, cand)
