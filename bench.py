@@ -5,8 +5,8 @@ Headline: one decode call of the B=1 workload at position 32767 (64 heads, head_
 top-k 512 of 8192 compressed entries, ratio 4, page size 64; the shape of the FreeToken PR 633
 "Kernel time" table), in microseconds per call, L2 flushed between calls.  The same JSON line
 carries the other workloads of the table (decode B=8 at ratios 128/4/0, prefill S=8192, the e4m3
-prefill chunk), the paged KV write and the compressor's gated pool at the same page's shapes, with
-their achieved GB/s or TFLOP/s against the measured GB300 peaks.
+prefill chunk), the paged KV write, the compressor's gated pool and the indexer logits at the
+pages' shapes, with their achieved GB/s or TFLOP/s against the measured GB300 peaks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                     [--workload NAME] [--no-sub | --sub NAME,...] [--no-cpu-baseline]
@@ -43,6 +43,23 @@ SUB_WORKLOADS = ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0", "prefill_s819
 KV_WRITES = {"kv_write_fp8_t65536": True, "kv_write_t65536": False}   # name -> e4m3 pool
 GATED_POOLS = {"gated_pool_b%d_r%d_d%d" % s: s for s in
                [(b, r, d) for b in (1, 8) for r in (8, 128) for d in (128, 512)]}
+# the indexer shapes of FreeToken PR 634 ("All shapes"): name -> (mode, n queries, first position,
+# ratio, sequences, candidates); decode shapes put each sequence's one query at ctx - 1
+INDEXERS = {
+    "indexer_full_prefill_n2048_start0_r2": ("full", 2048, 0, 2, 1, None),
+    "indexer_full_prefill_n8192_start0_r2": ("full", 8192, 0, 2, 1, None),
+    "indexer_full_prefill_n2048_start129024_r2": ("full", 2048, 129024, 2, 1, None),
+    "indexer_full_prefill_n128_start8064_r1": ("full", 128, 8064, 1, 1, None),
+    "indexer_full_prefill_n128_start130944_r1": ("full", 128, 130944, 1, 1, None),
+    "indexer_cand_prefill_n128_start8064_nc16384": ("cand", 128, 8064, 1, 1, 16384),
+    "indexer_cand_prefill_n128_start130944_nc16384": ("cand", 128, 130944, 1, 1, 16384),
+    "indexer_full_decode_b1_ctx32768_r2": ("full", 1, 32767, 2, 1, None),
+    "indexer_full_decode_b4_ctx32768_r2": ("full", 1, 32767, 2, 4, None),
+    "indexer_full_decode_b1_ctx131072_r2": ("full", 1, 131071, 2, 1, None),
+    "indexer_full_decode_b1_ctx131072_r1": ("full", 1, 131071, 1, 1, None),
+    "indexer_cand_decode_b1_ctx131072_nc16384": ("cand", 1, 131071, 1, 1, 16384),
+    "indexer_cand_decode_b4_ctx131072_nc16384": ("cand", 1, 131071, 1, 4, 16384),
+}
 FLUSH_BYTES = 512 << 20   # > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -396,6 +413,49 @@ def measure_gated_pool(name, device, steps, flush, peaks):
             "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
 
+def measure_indexer(name, device, flush, peaks):
+    """Indexer logits at one of the pages' shapes.  Work: 2·32·128 flop per (query, scored entry)
+    on the tensor cores; bytes: the packed key rows scored (68 B each, once per query group that
+    shares them), q, the weights and the logits written."""
+    import numpy as np
+    import torch
+    import sparse_paged_attention_gb300 as spa
+    from workloads import indexer_inputs
+    mode, n, start, ratio, B, nc = INDEXERS[name]
+    seqs = [np.arange(start, start + n)] * B
+    x = indexer_inputs(seqs, ratio, page_size=64, seed=5, cand_count=nc)
+    g = lambda t: None if t is None else t.to(device)
+    q, w, kp, bt, pos = g(x.q), g(x.weights), g(x.key_pool), g(x.block_table), g(x.positions)
+    cand, sot = g(x.cand), (g(x.seq_of_token) if B > 1 else None)
+    out = torch.empty((x.q.shape[0], x.num_cols), dtype=torch.float32, device=device)
+    call = lambda: spa.sparse_attn_indexer_logits(q, w, kp, bt, pos, ratio=ratio,
+                                                  num_cols=x.num_cols, cand=cand,
+                                                  seq_of_token=sot, num_seqs=B, out=out)
+    call()
+    if spa.sparse_attn_paged_check_errors():
+        raise RuntimeError(f"{name}: device error word")
+    big = n * x.num_cols >= (1 << 24)
+    times = time_device(call, 5 if big else 30, 3, flush)
+    us = 1e3 * statistics.mean(times)
+    warm = 1e3 * time_graph(call, reps=3 if big else 20, rounds=5)
+    p = x.positions.numpy().astype(np.int64)
+    if x.cand is None:
+        scored = np.minimum((p + 1) // ratio, x.num_cols)
+        rows = B * int(scored.max()) if n > 1 else int(scored.sum())
+    else:
+        c = x.cand.numpy().astype(np.int64)
+        scored = ((c >= 0) & (ratio * c + ratio - 1 <= p[:, None])).sum(axis=1)
+        rows = int(scored.sum())
+    flops = 2.0 * 32 * 128 * float(scored.sum())
+    nbytes = 68 * rows + x.q.numel() * 2 + x.weights.numel() * 4 + out.numel() * 4
+    tf = flops / (us * 1e-6) / 1e12
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "warm_l2_graph_us": round(warm, 3),
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+            "tflops": round(tf, 2), "frac_bf16_tensor": round(tf / peaks["bf16_tflops"], 4),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def cpu_baseline(name, seconds):
     """The float64 oracle as it stands, on the host cores, in a fresh process."""
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
@@ -486,6 +546,13 @@ def run_gpu(args):
             for name in filter(keep, GATED_POOLS):
                 try:
                     sub[name] = measure_gated_pool(name, device, 50, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - reported, not fatal
+                    sub[name] = {"error": str(e)[:300]}
+            # the indexer legs run only when named in --sub: its kernel has not yet been run
+            # to completion on a GPU
+            for name in (n for n in INDEXERS if only is not None and n in only):
+                try:
+                    sub[name] = measure_indexer(name, device, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
                     sub[name] = {"error": str(e)[:300]}
         # keep the GPU busy long enough for the clock sampler to see it under load
@@ -597,14 +664,15 @@ def main(argv=None):
     ap.add_argument("--no-sub", action="store_true", help="headline workload only")
     ap.add_argument("--sub", default=None,
                     help="comma-separated names: measure only these of the other workloads "
-                         "(attention workloads, kv_write_*, gated_pool_*)")
+                         "(attention workloads, kv_write_*, gated_pool_*, indexer_*)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.sub is not None:
-        unknown = set(args.sub.split(",")) - set(SUB_WORKLOADS) - set(KV_WRITES) - set(GATED_POOLS)
+        unknown = (set(args.sub.split(",")) - set(SUB_WORKLOADS) - set(KV_WRITES)
+                   - set(GATED_POOLS) - set(INDEXERS))
         if unknown:
             ap.error(f"unknown --sub workload(s): {sorted(unknown)}")
     if args.impl == "reference":

@@ -212,6 +212,39 @@ int sparse_attn_gated_pool(const float* kv, const float* gate, int32_t batch, in
                            int64_t gate_stride_b, int64_t gate_stride_r, void* out,
                            int32_t out_dtype, int64_t out_stride_b, void* stream);
 
+/*
+ * Indexer logits over packed fp4 key rows (FreeToken PR 634, "read dsv41 indexer key rows as
+ * int32 words": call path Indexer -> indexer_logits_packed; Full mode and candidate mode).
+ *   q:        device bf16 [num_tokens][num_heads][128], 16-byte aligned; num_heads must be 32.
+ *   weights:  device fp32 [num_tokens][num_heads], 4-byte aligned (per-head weights).
+ *   keys:     the index-key pool as an spa_pool_t: kv = packed rows, int32
+ *             [num_blocks][page_size][17], 4-byte aligned; k_scale, v_scale unused (NULL).  Row
+ *             format fp4_e8m0_b32: words 0..15 hold 128 OCP E2M1 codes (little-endian; byte i
+ *             holds element 2i in its low nibble, 2i + 1 in its high nibble), word 16 four OCP
+ *             E8M0 scale bytes, byte g scaling elements 32g .. 32g + 31.  Entry j of sequence b is
+ *             row block_table[b][j / page_size] * page_size + j % page_size.
+ *   positions, seq_of_token (NULL: every query in sequence 0), num_seqs: as for the attention.
+ *   ratio:    r >= 1; entry j is causal for a query at position p iff r*j + r - 1 <= p.
+ *   cand:     NULL for Full mode (column c scores entry c), else device int32
+ *             [num_tokens][num_cols] candidate entries (-1: none).
+ *   logits:   device fp32 [num_tokens][num_cols], 4-byte aligned:
+ *             logits[t][c] = sum_h w[t][h] * max(0, q[t][h][:] . k[j][:]), or -inf where the
+ *             entry is -1, not causal, or its page/block is invalid (which also sets SPA_ERR_INDEX
+ *             in the device error word).
+ * The logit formula is the reading this library takes (the page gives the key format and the
+ * head counts, not the formula).  The keys enter the contraction exactly (every code times its
+ * scale is a bf16 value, up to scale bytes of 252; larger products overflow to inf); q . k
+ * accumulates in fp32 on the tensor cores, the head sum in fp32.  Returns SPA_ERR_NULL,
+ * SPA_ERR_ALIGN, SPA_ERR_SHAPE (negative sizes, ratio < 1, bad pool geometry),
+ * SPA_ERR_UNSUPPORTED (num_heads != 32), SPA_ERR_CUDA.  Asynchronous on `stream`; allocates
+ * nothing.
+ */
+int sparse_attn_indexer_logits(const void* q, const float* weights, int32_t num_tokens,
+                               int32_t num_heads, const spa_pool_t* keys,
+                               const int32_t* positions, const int32_t* seq_of_token,
+                               int32_t num_seqs, int32_t ratio, const int32_t* cand,
+                               int32_t num_cols, float* logits, void* stream);
+
 /* Synchronises `stream`, returns the device error word (an OR of SPA_ERR_INDEX and
  * SPA_ERR_TIMEOUT, 0 if clean) accumulated since the last check on the current device, and
  * clears it.  Returns SPA_ERR_CUDA if the synchronisation itself fails. */

@@ -22,7 +22,7 @@ __all__ = [
     "sparse_attn_paged_prefill_fp8", "sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8",
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
     "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
-    "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool",
+    "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool", "sparse_attn_indexer_logits",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -99,6 +99,8 @@ def load_library():
     I64 = ctypes.c_int64
     lib.sparse_attn_gated_pool.argtypes = [P, P, I32, I32, I32, I64, I64, I64, I64, P, I32, I64, P]
     lib.sparse_attn_gated_pool.restype = ctypes.c_int
+    lib.sparse_attn_indexer_logits.argtypes = [P, P, I32, I32, PP, P, P, I32, I32, P, I32, P, P]
+    lib.sparse_attn_indexer_logits.restype = ctypes.c_int
     lib.sparse_attn_paged_check_errors.argtypes = [P]
     lib.sparse_attn_paged_check_errors.restype = ctypes.c_int
     lib.sparse_attn_paged_strerror.argtypes = [ctypes.c_int]
@@ -297,6 +299,46 @@ def sparse_attn_gated_pool(kv, gate, out=None, *, out_dtype=torch.float32, strea
                                     dt, out.stride(0), _stream(stream))
     if st != 0:
         raise SpaError(st, "sparse_attn_gated_pool")
+    return out
+
+
+def sparse_attn_indexer_logits(q, weights, key_pool, block_table, positions, *, ratio,
+                               num_cols=None, cand=None, seq_of_token=None, num_seqs=None,
+                               out=None, stream=None):
+    """Indexer logits over packed fp4_e8m0_b32 key rows (int32 [num_blocks, page_size, 17]):
+    ``logits[t, c] = sum_h weights[t, h] * relu(q[t, h] . k[j])`` with j = c (Full mode) or
+    ``cand[t, c]``; -inf where the entry does not exist.  Returns fp32 [T, num_cols]."""
+    lib = load_library()
+    if q.dtype != torch.bfloat16 or q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 [T, heads, 128] tensor")
+    if weights.dtype != torch.float32 or tuple(weights.shape) != tuple(q.shape[:2]) or \
+            not weights.is_contiguous():
+        raise ValueError("weights must be a contiguous fp32 [T, heads] tensor")
+    if key_pool.dtype != torch.int32 or key_pool.dim() != 3 or key_pool.shape[2] != 17 or \
+            not key_pool.is_contiguous():
+        raise ValueError("key_pool must be a contiguous int32 [num_blocks, page_size, 17] tensor")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or \
+            not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [num_seqs, stride] tensor")
+    for name, t in (("positions", positions), ("seq_of_token", seq_of_token), ("cand", cand)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 tensor")
+    T, H = int(q.shape[0]), int(q.shape[1])
+    if cand is not None:
+        num_cols = int(cand.shape[1])
+    if num_cols is None:
+        raise ValueError("Full mode needs num_cols")
+    if out is None:
+        out = torch.empty((T, num_cols), dtype=torch.float32, device=q.device)
+    B = int(block_table.shape[0]) if num_seqs is None else int(num_seqs)
+    pool = SpaPoolC(key_pool.data_ptr(), None, None, block_table.data_ptr(), key_pool.shape[0],
+                    key_pool.shape[1], block_table.shape[1])
+    st = lib.sparse_attn_indexer_logits(q.data_ptr(), weights.data_ptr(), T, H,
+                                        ctypes.byref(pool), positions.data_ptr(),
+                                        _ptr(seq_of_token), B, int(ratio), _ptr(cand),
+                                        int(num_cols), out.data_ptr(), _stream(stream))
+    if st != 0:
+        raise SpaError(st, "sparse_attn_indexer_logits")
     return out
 
 

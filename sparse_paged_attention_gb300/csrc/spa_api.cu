@@ -479,6 +479,52 @@ int sparse_attn_gated_pool(const float* kv, const float* gate, int32_t batch, in
   return SPA_OK;
 }
 
+int sparse_attn_indexer_logits(const void* q, const float* weights, int32_t num_tokens,
+                               int32_t num_heads, const spa_pool_t* keys,
+                               const int32_t* positions, const int32_t* seq_of_token,
+                               int32_t num_seqs, int32_t ratio, const int32_t* cand,
+                               int32_t num_cols, float* logits, void* stream) {
+  if (num_tokens < 0 || num_cols < 0 || num_seqs < 1 || ratio < 1 || num_heads < 1)
+    return SPA_ERR_SHAPE;
+  if (num_heads != spa::kIdxHeads) return SPA_ERR_UNSUPPORTED;
+  if (num_tokens == 0 || num_cols == 0) return SPA_OK;
+  if (!q || !weights || !keys || !keys->kv || !keys->block_table || !positions || !logits)
+    return SPA_ERR_NULL;
+  if (keys->num_blocks < 1 || keys->page_size < 1 || keys->bt_stride < 1) return SPA_ERR_SHAPE;
+  const auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!aligned16(q) || !a4(weights) || !a4(keys->kv) || !a4(logits)) return SPA_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  const int ds = current_device(&dev, &sms);
+  if (ds) return ds;
+  spa::IndexerArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = static_cast<const uint16_t*>(q);
+  a.w = weights;
+  a.keys = static_cast<const int32_t*>(keys->kv);
+  a.bt = keys->block_table;
+  a.positions = positions;
+  a.seq_of_token = seq_of_token;
+  a.cand = cand;
+  a.logits = logits;
+  a.num_blocks = keys->num_blocks;
+  a.T = num_tokens;
+  a.B = num_seqs;
+  a.ps = keys->page_size;
+  a.bt_stride = keys->bt_stride;
+  a.ratio = ratio;
+  a.ncols = num_cols;
+  // queries share a key tile only when they share a sequence: with no sequence ids every query
+  // is in sequence 0 and groups of eight share each tile; otherwise (and in candidate mode, where
+  // every query has its own entries) one query per group
+  a.nq = (cand || seq_of_token) ? 1 : (num_tokens < spa::kIdxMaxQ ? num_tokens : spa::kIdxMaxQ);
+  a.ntiles = (num_cols + spa::kIdxTile - 1) / spa::kIdxTile;
+  a.nunits = (long long)((num_tokens + a.nq - 1) / a.nq) * a.ntiles;
+  const cudaError_t e = spa::launch_indexer(a, cand != nullptr, sms,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "indexer kernel launch");
+  return SPA_OK;
+}
+
 int sparse_attn_paged_kv_write(const void* k, const void* v, int32_t num_tokens, int32_t head_dim,
                                const int32_t* positions, const int32_t* seq_of_token,
                                int32_t num_seqs, const spa_pool_t* pool, void* stream) {
@@ -503,7 +549,10 @@ int sparse_attn_paged_check_errors(void* stream) {
   int w = 0;
   e = spa::read_and_clear_kv_write_error_word(&w);
   if (e != cudaSuccess) return cuda_fail(e, "device error word");
-  return v | w;
+  int x = 0;
+  e = spa::read_and_clear_indexer_error_word(&x);
+  if (e != cudaSuccess) return cuda_fail(e, "device error word");
+  return v | w | x;
 }
 
 const char* sparse_attn_paged_strerror(int status) {

@@ -1,0 +1,259 @@
+// spa_indexer.cu - indexer logits over packed fp4 key rows (FreeToken PR 634, "Changes": key rows
+// of 17 int32 words, 16 of e2m1 codes and one of ue8m0 scales, one scale per 32 elements, index
+// head_dim 128; "Kernel time": 32 index heads; Full and candidate modes).
+//
+//   logit[t][c] = sum_h w[t][h] * max(0, q[t][h][:] . k[j][:]),   j = c (full) or cand[t][c]
+//
+// and -inf where entry j does not exist for query t (-1, non-causal: r*j + r - 1 > pos, or an
+// invalid page, which also raises SPA_ERR_INDEX).
+//
+// The contraction runs on the tensor cores: a tile of 128 key rows is the MMA's M side, a group
+// of up to eight queries' 32 heads its N side (N = 32 per query, up to 256) and the 128 dims its
+// K, as tcgen05 kind::f16 with both operands bf16 in 128-byte-swizzled shared memory and the
+// scores fp32 in TMEM.  The key rows are dequantised on the way into shared memory: every e2m1
+// code times its ue8m0 scale is exactly a bf16 value (two significant bits times a power of two),
+// so the keys enter the MMA unrounded.  The epilogue reads one key row's scores per thread
+// (TMEM lane = key row), applies the ReLU and the head weights, and writes one logit per query.
+//
+// A CTA of four warps runs its units (query group, key tile) one after the other: load and
+// dequantise, MMA, epilogue.  Units of one query group are contiguous in a CTA's range, so its
+// queries stay in shared memory across tiles; full-mode tiles past every query's causal limit are
+// written as -inf without an MMA.
+#include <cuda_bf16.h>
+
+#include "spa_launch.h"
+
+namespace spa {
+
+namespace {
+
+constexpr int kTile = kIdxTile;            // key rows per unit (MMA M)
+constexpr int kAAtom = kTile * 128;        // bytes of one 64-dim column of the key tile
+constexpr int kBAtom = kIdxMaxN * 128;     // bytes of one 64-dim column of the query tile
+constexpr int kAOff = 0;
+constexpr int kBOff = 2 * kAAtom;                          // 32 KB
+constexpr int kWOff = kBOff + 2 * kBAtom;                  // 96 KB: weights [8][32] fp32
+constexpr int kPosOff = kWOff + kIdxMaxQ * kIdxHeads * 4;  // positions [8], sequences [8]
+constexpr int kBarOff = kPosOff + 2 * kIdxMaxQ * 4;        // mbarrier (8 B), tmem base, abort
+constexpr int kSmemUsed = kBarOff + 64;
+constexpr uint32_t kTmemCols = 256;
+
+// e2m1 code (4 bits) times a scale -> bf16 bits.  The magnitude is built from the code's fields
+// ((1 + m/2) 2^(e-1), or m/2 for e = 0), the product with a power of two is exact in fp32 (down to
+// fp32 subnormals; past the fp32 range it is inf), and the bf16 conversion of an exact value with
+// two significant bits is exact.  Bit 3 is the sign.
+__device__ __forceinline__ uint32_t e2m1_to_bf16_bits(uint32_t c, float scale) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
+  const float v = __uint_as_float(mag) * scale;
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) | ((c & 8u) << 12);
+}
+
+// ue8m0 scale byte -> fp32: 2^(s - 127); 0 is the fp32 subnormal 2^-127; 0xFF is NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  if (s == 0u) return __uint_as_float(0x00400000u);
+  if (s == 255u) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(s << 23);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <bool kCand>
+__global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerArgs p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  float* s_w = reinterpret_cast<float*>(sm + kWOff);
+  int* s_pos = reinterpret_cast<int*>(sm + kPosOff);
+  int* s_seq = s_pos + kIdxMaxQ;
+  const uint32_t bar = sb + kBarOff;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBarOff + 16);
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();  // lane 0 of warp 0 took the branch above; the allocation is warp-collective
+  if (warp == 0) tmem_alloc(sb + kBarOff + 8, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kBarOff + 8);
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+
+  const int nq = p.nq, N = nq * kIdxHeads;
+  const uint32_t idesc = idesc_bf16(kTile, N, 0, 0);
+  const long long u0 = (long long)blockIdx.x * p.nunits / gridDim.x;
+  const long long u1 = (long long)(blockIdx.x + 1) * p.nunits / gridDim.x;
+  long long cur_group = -1;
+  uint32_t phase = 0;
+
+  for (long long u = u0; u < u1; ++u) {
+    const long long g = u / p.ntiles;
+    const int tile = (int)(u % p.ntiles);
+    const int q0 = (int)(g * nq);
+    const int nqg = min(nq, p.T - q0);
+
+    if (g != cur_group) {  // the previous unit's MMA has completed: the query tile is free
+      const int chunks = N * 16;  // 16-byte chunks of the N query rows (8 dims each)
+      for (int idx = tid; idx < chunks; idx += kIdxThreads) {
+        const int n = idx >> 4, k = idx & 15;
+        const int ql = n / kIdxHeads, h = n % kIdxHeads;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ql < nqg)
+          v = __ldg(reinterpret_cast<const uint4*>(
+              p.q + ((size_t)(q0 + ql) * kIdxHeads + h) * kIdxDim + k * 8));
+        st_shared_v4(sb + kBOff + (k >> 3) * kBAtom + n * 128 + (((k & 7) ^ (n & 7)) << 4), v.x,
+                     v.y, v.z, v.w);
+      }
+      for (int idx = tid; idx < nq * kIdxHeads; idx += kIdxThreads) {
+        const int ql = idx / kIdxHeads;
+        s_w[idx] = ql < nqg ? __ldg(p.w + (size_t)q0 * kIdxHeads + idx) : 0.f;
+      }
+      if (tid < kIdxMaxQ) {
+        const bool live = tid < nqg;
+        s_pos[tid] = live ? __ldg(p.positions + q0 + tid) : -1;
+        s_seq[tid] = live ? (p.seq_of_token ? __ldg(p.seq_of_token + q0 + tid) : 0) : 0;
+      }
+      cur_group = g;
+    }
+    __syncthreads();
+
+    int max_pos = -1;
+    for (int ql = 0; ql < nqg; ++ql) max_pos = max(max_pos, s_pos[ql]);
+    const long long causal_entries = max_pos < 0 ? 0 : ((long long)max_pos + 1) / p.ratio;
+    const int c = tile * kTile + tid;
+
+    if (!kCand && (long long)tile * kTile >= causal_entries) {
+      // no query of the group reaches this tile: all -inf, no MMA (uniform over the CTA)
+      if (c < p.ncols)
+        for (int ql = 0; ql < nqg; ++ql)
+          p.logits[(size_t)(q0 + ql) * p.ncols + c] = -INFINITY;
+      __syncthreads();
+      continue;
+    }
+
+    // this thread's key row: entry j, resolved through the sequence's block table
+    long long j = -1, row = -1;
+    if (c < p.ncols) j = kCand ? (long long)__ldg(p.cand + (size_t)q0 * p.ncols + c) : c;
+    if (j >= 0 && j < causal_entries) {
+      const int b = s_seq[0];
+      const long long page = j / p.ps;
+      bool ok = b >= 0 && b < p.B && page < p.bt_stride;
+      if (ok) {
+        const int blk = __ldg(p.bt + (size_t)b * p.bt_stride + page);
+        ok = blk >= 0 && (long long)blk < p.num_blocks;
+        if (ok) row = (long long)blk * p.ps + j % p.ps;
+      }
+      if (!ok) flag_error(SPA_ERR_INDEX);
+    }
+    {
+      uint32_t words[kIdxRowWords];
+      if (row >= 0) {
+        const int32_t* src = p.keys + row * kIdxRowWords;
+#pragma unroll
+        for (int w = 0; w < kIdxRowWords; ++w) words[w] = (uint32_t)__ldg(src + w);
+      } else {
+#pragma unroll
+        for (int w = 0; w < kIdxRowWords; ++w) words[w] = 0u;
+        words[kIdxRowWords - 1] = 0x7F7F7F7Fu;  // scale 1: the row's scores are 0, then masked
+      }
+      float scale[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) scale[s] = e8m0_to_f32((words[16] >> (8 * s)) & 0xFFu);
+#pragma unroll
+      for (int w = 0; w < 16; ++w) {  // word w: dims 8w .. 8w+7, one 16-byte chunk of the row
+        const float sc = scale[w >> 2];
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t byte = (words[w] >> (8 * e)) & 0xFFu;
+          pk[e] = e2m1_to_bf16_bits(byte & 0xFu, sc) | (e2m1_to_bf16_bits(byte >> 4, sc) << 16);
+        }
+        st_shared_v4(sb + kAOff + (w >> 3) * kAAtom + tid * 128 + (((w & 7) ^ (tid & 7)) << 4),
+                     pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      tc_fence_after();
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {  // K = 128 in steps of 16: two 64-dim columns of 4 steps
+        const uint64_t da = sdesc(sb + kAOff + (s >> 2) * kAAtom + (s & 3) * 32, 16, 1024);
+        const uint64_t db = sdesc(sb + kBOff + (s >> 2) * kBAtom + (s & 3) * 32, 16, 1024);
+        mma_bf16(tmem, da, db, idesc, s > 0 ? 1u : 0u);
+      }
+      mma_commit(bar);
+    }
+    const bool done = mbar_wait(bar, phase, abort_flag);
+    phase ^= 1u;
+    if (!__syncthreads_and(done)) break;  // a wait gave up: SPA_ERR_TIMEOUT is set
+    tc_fence_after();
+
+    // tcgen05.ld and tcgen05.wait::ld are warp-collective (.sync.aligned): every lane of every
+    // warp runs them, converged, whatever its column; only the store depends on the column
+    __syncwarp();
+    for (int ql = 0; ql < nqg; ++ql) {
+      float v[32];
+      tmem_ld32(lane_base + ql * kIdxHeads, v);
+      tmem_wait_ld();
+      float acc = 0.f;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) acc = fmaf(s_w[ql * kIdxHeads + h], fmaxf(v[h], 0.f), acc);
+      const bool causal = row >= 0 && (long long)p.ratio * j + p.ratio - 1 <= s_pos[ql];
+      if (c < p.ncols) p.logits[(size_t)(q0 + ql) * p.ncols + c] = causal ? acc : -INFINITY;
+    }
+    tc_fence_before();
+    __syncthreads();  // scores read and key tile consumed before the next unit overwrites them
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+// This translation unit's copy of the device error word (see spa_device.cuh).
+cudaError_t read_and_clear_indexer_error_word(int* value) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_spa_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_spa_error, &zero, sizeof(int));
+}
+
+int indexer_smem_bytes() { return kSmemUsed + 1024; }
+
+cudaError_t launch_indexer(const IndexerArgs& a, bool cand, int num_sms, cudaStream_t stream) {
+  if (a.nunits == 0) return cudaSuccess;
+  const int smem = indexer_smem_bytes();
+  cudaError_t e = cand ? cudaFuncSetAttribute(indexer_kernel<true>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                       : cudaFuncSetAttribute(indexer_kernel<false>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // two CTAs per SM (about 100 KB of shared memory and 256 TMEM columns each)
+  const long long grid = a.nunits < 2LL * num_sms ? a.nunits : 2LL * num_sms;
+  if (cand)
+    indexer_kernel<true><<<(unsigned)grid, kIdxThreads, smem, stream>>>(a);
+  else
+    indexer_kernel<false><<<(unsigned)grid, kIdxThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace spa

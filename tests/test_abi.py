@@ -122,3 +122,23 @@ def test_gated_pool_host_validation(lib, no_device):
     assert call(kv=None) == S["SPA_ERR_NULL"] and call(out=None) == S["SPA_ERR_NULL"]
     assert call(kv=kv + 2) == S["SPA_ERR_ALIGN"] and call(g=g + 1) == S["SPA_ERR_ALIGN"]
     assert call(out=out + 2) == S["SPA_ERR_ALIGN"]                   # fp32 out: 4-byte aligned
+
+
+def test_indexer_host_validation(lib, no_device):
+    S = spa.SPA_STATUS
+    f = lib.sparse_attn_indexer_logits
+    keys = SpaPoolC(0x1000, None, None, 0x2000, 64, 64, 16)
+    q, w, pos, out = 0x3000, 0x4000, 0x5000, 0x6000
+
+    def call(q=q, w=w, T=4, H=32, keys=keys, pos=pos, B=1, r=2, cand=None, n=1024, out=out):
+        return f(q, w, T, H, ctypes.byref(keys) if keys is not None else None, pos, None, B, r,
+                 cand, n, out, None)
+    assert call(T=-1) == S["SPA_ERR_SHAPE"] and call(n=-1) == S["SPA_ERR_SHAPE"]
+    assert call(r=0) == S["SPA_ERR_SHAPE"] and call(B=0) == S["SPA_ERR_SHAPE"]
+    assert call(H=16) == S["SPA_ERR_UNSUPPORTED"]
+    assert call(T=0) == S["SPA_OK"] and call(n=0) == S["SPA_OK"]          # nothing to do
+    assert call(q=None) == S["SPA_ERR_NULL"] and call(keys=None) == S["SPA_ERR_NULL"]
+    assert call(out=None) == S["SPA_ERR_NULL"]
+    assert call(q=q + 8) == S["SPA_ERR_ALIGN"] and call(out=out + 2) == S["SPA_ERR_ALIGN"]
+    assert call(keys=SpaPoolC(0x1002, None, None, 0x2000, 64, 64, 16)) == S["SPA_ERR_ALIGN"]
+    assert call(keys=SpaPoolC(0x1000, None, None, 0x2000, 0, 64, 16)) == S["SPA_ERR_SHAPE"]
