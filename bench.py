@@ -121,19 +121,27 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources with comments and blank space removed: a counter capture stays
-    valid across comment edits, and no longer once any code changes."""
+    """Hash of what compiles into the attention kernel, with comments and blank space removed: its
+    translation unit (spa_attention.cu), the library headers it includes (spa_launch.h,
+    spa_device.cuh) and, of the public header, the status codes the kernel raises.  A counter
+    capture stays valid across comment edits and changes to other kernels or to host code, and no
+    longer once any of this code changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_paged_attention_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
-                    + glob.glob(os.path.join(csrc, "*.h"))):
-        with open(p, encoding="utf-8") as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        text = " ".join(text.split())
-        h.update(os.path.basename(p).encode() + text.encode())
+    for name in ("spa_attention.cu", "spa_device.cuh", "spa_launch.h"):
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
+    with open(os.path.join(ROOT, "include", "sparse_attn_paged.h"), encoding="utf-8") as f:
+        pub = _code_only(f.read())
+    m = re.search(r"typedef enum spa_status \{.*?\} spa_status_t;", pub)
+    h.update(b"spa_status" + (m.group(0).encode() if m else b""))
     return h.hexdigest()[:16]
 
 

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "sparse_attn_paged.h"
+#include "spa_indexer.h"
 #include "spa_launch.h"
 
 namespace {

@@ -21,7 +21,7 @@
 // written as -inf without an MMA.
 #include <cuda_bf16.h>
 
-#include "spa_launch.h"
+#include "spa_indexer.h"
 
 namespace spa {
 
