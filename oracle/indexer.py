@@ -32,7 +32,9 @@ Readings (the pages print neither the logit formula nor the row's byte order):
 Parity status: the format decoding is pinned to the OCP definitions and hand-worked rows
 (tests/test_oracle_indexer.py, tests/golden/e2m1_codes.json); the logit formula is a reading,
 pinned by closed forms (unit queries read single key elements, ReLU clips negative scores, the
-weights act linearly) and by the identity between candidate and full mode.
+weights act linearly) and by the identity between candidate and full mode.  The top-k selection
+(``topk_entries``) is pinned by a brute-force sort with many ties and by the validity of its lists
+as attention top-k lists.
 """
 import numpy as np
 
@@ -126,3 +128,27 @@ def indexer_logits(q_bits, weights, key_pool, block_table, positions, seq_ids, *
         s = k @ q[t].T                                     # [n_cols, H] per-head scores
         out[n, np.asarray(cols)] = np.maximum(s, 0.0) @ wts[t]
     return out, error
+
+
+def topk_entries(logits, k: int, cand=None) -> np.ndarray:
+    """The top-k selection that follows the logits: for each query, the k scored entries with the
+    largest logits, in decreasing order of logit, ties going to the smaller entry index; -1 fills
+    the list when fewer than k entries were scored (finite logit).  ``cand`` maps candidate
+    columns to entry ids (Full mode: column c is entry c).  Returns int32 [T, k], usable as the
+    attention's top-k list.
+
+    Reading: the page names a top-k step after the logits (its test list has a top-k test) but
+    prints no rule; this is the plain one, with the tie rule made explicit so that the list is
+    unique.
+    """
+    lg = np.asarray(logits, dtype=np.float64)
+    T, n = lg.shape
+    ids = np.broadcast_to(np.arange(n), (T, n)) if cand is None else np.asarray(cand, np.int64)
+    out = np.full((T, k), -1, dtype=np.int32)
+    for t in range(T):
+        ok = np.isfinite(lg[t])
+        vals, ents = lg[t][ok], ids[t][ok]
+        order = np.lexsort((ents, -vals))          # by logit descending, then entry ascending
+        take = order[:k]
+        out[t, :len(take)] = ents[take]
+    return out

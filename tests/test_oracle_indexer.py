@@ -255,3 +255,61 @@ def test_pins_catch_off_by_one_causality(monkeypatch):
         return real(*a, ratio=ratio, **kw)
     monkeypatch.setattr(oi, "indexer_logits", wrong)
     assert _some_pin_fails()
+
+
+# ---------------------------------------------------------------------------------------------
+# top-k selection
+# ---------------------------------------------------------------------------------------------
+def _brute_topk(row, ids, k):
+    scored = [(float(v), int(j)) for v, j in zip(row, ids) if np.isfinite(v)]
+    best = sorted(scored, key=lambda vj: (-vj[0], vj[1]))[:k]
+    return [j for _, j in best] + [-1] * (k - len(best))
+
+
+def test_topk_matches_a_brute_force_sort():
+    rng = np.random.default_rng(20)
+    lg = rng.integers(-4, 5, size=(30, 50)).astype(np.float64)     # many ties
+    lg[rng.random(lg.shape) < 0.3] = -np.inf
+    for k in (1, 7, 50, 64):
+        got = oi.topk_entries(lg, k)
+        for t in range(30):
+            assert got[t].tolist() == _brute_topk(lg[t], range(50), k), (k, t)
+
+
+def test_topk_candidate_ids_and_order_invariance():
+    rng = np.random.default_rng(21)
+    ids = np.stack([rng.permutation(1000)[:40] for _ in range(5)])
+    lg = np.round(rng.standard_normal((5, 40)), 1)
+    got = oi.topk_entries(lg, 12, cand=ids)
+    for t in range(5):
+        assert got[t].tolist() == _brute_topk(lg[t], ids[t], 12)
+        perm = rng.permutation(40)
+        again = oi.topk_entries(lg[t:t + 1, perm], 12, cand=ids[t:t + 1, perm])
+        assert np.array_equal(again[0], got[t])
+
+
+def test_topk_of_indexer_logits_feeds_the_attention():
+    """The indexer's top-k lists are valid attention top-k lists: distinct, causal entries, -1
+    only at the tail."""
+    x = indexer_inputs([np.arange(0, 200)], 4, num_heads=4, page_size=8, seed=22)
+    lg, _ = oi.indexer_logits(bf16_bits(x.q), x.weights.numpy(), x.key_pool.numpy(),
+                              x.block_table.numpy(), x.positions.numpy(), x.seq_ids(), ratio=4,
+                              num_cols=x.num_cols)
+    tk = oi.topk_entries(lg, 16)
+    for t, p in enumerate(range(200)):
+        valid = (p + 1) // 4
+        row = tk[t]
+        n = int((row >= 0).sum())
+        assert n == min(16, valid) and (row[n:] == -1).all()
+        assert len(set(row[:n].tolist())) == n and (4 * row[:n] + 3 <= p).all()
+        assert np.all(np.diff(lg[t, row[:n]]) <= 0)
+
+
+def test_pins_catch_ties_to_the_larger_index(monkeypatch):
+    real_lexsort = np.lexsort
+    monkeypatch.setattr(oi.np, "lexsort", lambda keys: real_lexsort((-keys[0], keys[1])))
+    try:
+        with pytest.raises(AssertionError):
+            test_topk_matches_a_brute_force_sort()
+    finally:
+        monkeypatch.undo()
