@@ -245,6 +245,22 @@ int sparse_attn_indexer_logits(const void* q, const float* weights, int32_t num_
                                int32_t num_seqs, int32_t ratio, const int32_t* cand,
                                int32_t num_cols, float* logits, void* stream);
 
+/*
+ * Top-k selection over indexer logits (the step after sparse_attn_indexer_logits; FreeToken PR 634
+ * lists a top-k test beside the logits kernel).  For each query t: the k entries with the largest
+ * finite logits[t][c], in decreasing order of logit, ties going to the smaller entry index; -1
+ * fills the row when fewer than k logits are finite (-inf and NaN are "not scored").  Column c is
+ * entry c, or cand[t][c] when cand is given (as for the logits).  -0 and +0 are equal logits.
+ *   logits:   device fp32 [num_tokens][num_cols]; cand: device int32 [num_tokens][num_cols] or
+ *             NULL; topk_idx: device int32 [num_tokens][k], the attention's top-k list.
+ *   k:        0 .. 2048 (SPA_ERR_UNSUPPORTED above).
+ * The selection is exact (integer comparisons of the logits' bits and the entry indices).  Returns
+ * SPA_ERR_SHAPE for negative sizes, SPA_ERR_NULL, SPA_ERR_ALIGN (4-byte alignment), SPA_ERR_CUDA.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+int sparse_attn_indexer_topk(const float* logits, int32_t num_tokens, int32_t num_cols,
+                             const int32_t* cand, int32_t k, int32_t* topk_idx, void* stream);
+
 /* Synchronises `stream`, returns the device error word (an OR of SPA_ERR_INDEX and
  * SPA_ERR_TIMEOUT, 0 if clean) accumulated since the last check on the current device, and
  * clears it.  Returns SPA_ERR_CUDA if the synchronisation itself fails. */

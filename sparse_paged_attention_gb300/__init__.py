@@ -23,6 +23,7 @@ __all__ = [
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
     "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
     "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool", "sparse_attn_indexer_logits",
+    "sparse_attn_indexer_topk",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -101,6 +102,8 @@ def load_library():
     lib.sparse_attn_gated_pool.restype = ctypes.c_int
     lib.sparse_attn_indexer_logits.argtypes = [P, P, I32, I32, PP, P, P, I32, I32, P, I32, P, P]
     lib.sparse_attn_indexer_logits.restype = ctypes.c_int
+    lib.sparse_attn_indexer_topk.argtypes = [P, I32, I32, P, I32, P, P]
+    lib.sparse_attn_indexer_topk.restype = ctypes.c_int
     lib.sparse_attn_paged_check_errors.argtypes = [P]
     lib.sparse_attn_paged_check_errors.restype = ctypes.c_int
     lib.sparse_attn_paged_strerror.argtypes = [ctypes.c_int]
@@ -339,6 +342,26 @@ def sparse_attn_indexer_logits(q, weights, key_pool, block_table, positions, *, 
                                         int(num_cols), out.data_ptr(), _stream(stream))
     if st != 0:
         raise SpaError(st, "sparse_attn_indexer_logits")
+    return out
+
+
+def sparse_attn_indexer_topk(logits, k, *, cand=None, out=None, stream=None):
+    """The k entries with the largest finite logits per row (fp32 [T, N]), in decreasing order of
+    logit, ties to the smaller entry, -1 fill; column c is entry c or ``cand[t, c]``.  Returns
+    int32 [T, k], usable as the attention's top-k list."""
+    lib = load_library()
+    if logits.dtype != torch.float32 or logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous fp32 [T, N] tensor")
+    if cand is not None and (cand.dtype != torch.int32 or cand.shape != logits.shape or
+                             not cand.is_contiguous()):
+        raise ValueError("cand must be a contiguous int32 tensor shaped like logits")
+    T, N = int(logits.shape[0]), int(logits.shape[1])
+    if out is None:
+        out = torch.empty((T, int(k)), dtype=torch.int32, device=logits.device)
+    st = lib.sparse_attn_indexer_topk(logits.data_ptr(), T, N, _ptr(cand), int(k),
+                                      out.data_ptr(), _stream(stream))
+    if st != 0:
+        raise SpaError(st, "sparse_attn_indexer_topk")
     return out
 
 

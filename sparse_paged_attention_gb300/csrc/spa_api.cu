@@ -526,6 +526,30 @@ int sparse_attn_indexer_logits(const void* q, const float* weights, int32_t num_
   return SPA_OK;
 }
 
+int sparse_attn_indexer_topk(const float* logits, int32_t num_tokens, int32_t num_cols,
+                             const int32_t* cand, int32_t k, int32_t* topk_idx, void* stream) {
+  if (num_tokens < 0 || num_cols < 0 || k < 0) return SPA_ERR_SHAPE;
+  if (k > spa::kIdxTopkMax) return SPA_ERR_UNSUPPORTED;
+  if (num_tokens == 0 || k == 0) return SPA_OK;
+  if (!topk_idx || (num_cols > 0 && !logits)) return SPA_ERR_NULL;
+  const auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!a4(logits) || !a4(cand) || !a4(topk_idx)) return SPA_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  const int ds = current_device(&dev, &sms);
+  if (ds) return ds;
+  spa::TopkArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.logits = logits;
+  a.cand = cand;
+  a.topk = topk_idx;
+  a.T = num_tokens;
+  a.ncols = num_cols;
+  a.k = k;
+  const cudaError_t e = spa::launch_topk(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "top-k kernel launch");
+  return SPA_OK;
+}
+
 int sparse_attn_paged_kv_write(const void* k, const void* v, int32_t num_tokens, int32_t head_dim,
                                const int32_t* positions, const int32_t* seq_of_token,
                                int32_t num_seqs, const spa_pool_t* pool, void* stream) {

@@ -33,4 +33,15 @@ int indexer_smem_bytes();
 cudaError_t launch_indexer(const IndexerArgs& a, bool cand, int num_sms, cudaStream_t stream);
 cudaError_t read_and_clear_indexer_error_word(int* value);
 
+// Top-k selection over the logits rows.
+constexpr int kIdxTopkMax = 2048;
+struct TopkArgs {
+  const float* logits;   // [T][ncols], -inf where no entry was scored
+  const int32_t* cand;   // [T][ncols] entry ids of the columns, or NULL (column c is entry c)
+  int32_t* topk;         // [T][k]
+  long long T;
+  int ncols, k;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
+
 }  // namespace spa

@@ -142,3 +142,17 @@ def test_indexer_host_validation(lib, no_device):
     assert call(q=q + 8) == S["SPA_ERR_ALIGN"] and call(out=out + 2) == S["SPA_ERR_ALIGN"]
     assert call(keys=SpaPoolC(0x1002, None, None, 0x2000, 64, 64, 16)) == S["SPA_ERR_ALIGN"]
     assert call(keys=SpaPoolC(0x1000, None, None, 0x2000, 0, 64, 16)) == S["SPA_ERR_SHAPE"]
+
+
+def test_topk_host_validation(lib, no_device):
+    S = spa.SPA_STATUS
+    f = lib.sparse_attn_indexer_topk
+    assert f(0x1000, -1, 10, None, 4, 0x2000, None) == S["SPA_ERR_SHAPE"]
+    assert f(0x1000, 2, 10, None, -1, 0x2000, None) == S["SPA_ERR_SHAPE"]
+    assert f(0x1000, 2, 10, None, 4096, 0x2000, None) == S["SPA_ERR_UNSUPPORTED"]
+    assert f(0x1000, 0, 10, None, 4, 0x2000, None) == S["SPA_OK"]
+    assert f(0x1000, 2, 10, None, 0, 0x2000, None) == S["SPA_OK"]
+    assert f(None, 2, 10, None, 4, 0x2000, None) == S["SPA_ERR_NULL"]
+    assert f(0x1000, 2, 10, None, 4, None, None) == S["SPA_ERR_NULL"]
+    assert f(0x1002, 2, 10, None, 4, 0x2000, None) == S["SPA_ERR_ALIGN"]
+    assert f(0x1000, 2, 10, 0x3001, 4, 0x2000, None) == S["SPA_ERR_ALIGN"]

@@ -1,4 +1,4 @@
-"""Indexer logits on the GPU against the float64 oracle, element by element.
+"""Indexer logits and their top-k selection on the GPU against the float64 oracle.
 
 Shapes follow FreeToken PR 634 ("Kernel time": 32 index heads, index head_dim 128, Full mode and
 candidate mode, prefill and decode), scaled so the oracle finishes in seconds, plus the pages'
@@ -20,13 +20,14 @@ import sparse_paged_attention_gb300 as spa
 from oracle import indexer as oi
 from workloads import bf16_bits, indexer_inputs
 
-# The indexer kernel has not yet run to completion on a GPU.  Its first run hung: the epilogue
-# ran the warp-collective tcgen05.ld under a per-lane column test, so a warp straddling the last
-# column of a ragged tile diverged on it.  That was found by reading and fixed (every lane now
-# loads, only the store is guarded), but the fixed kernel has not been run since; these tests stay
-# skipped until it has, once, on the smallest case.
+# The indexer kernels have not yet run to completion on a GPU.  The logits kernel's first run
+# hung: its epilogue ran the warp-collective tcgen05.ld under a per-lane column test, so a warp
+# straddling the last column of a ragged tile diverged on it.  That was found by reading and fixed
+# (every lane now loads, only the store is guarded), but the fixed kernel has not been run since,
+# and the top-k kernel has never run; these tests stay skipped until both have, once, on the
+# smallest case.
 pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="indexer kernel not yet run to completion on a GPU")]
+              pytest.mark.skip(reason="indexer kernels not yet run to completion on a GPU")]
 
 
 def _dev():
@@ -164,3 +165,40 @@ def test_pages_full_prefill_shape_sampled():
     got, st = _run(x, _dev())
     assert st == 0
     _compare(x, got, np.array([0, 7, 8, 64, 127]))
+
+
+# ---------------------------------------------------------------------------------------------
+# top-k selection: exact against the oracle on seeded logits (ties, -inf, -0, few scored rows)
+# ---------------------------------------------------------------------------------------------
+def _topk_logits(T, N, seed, kind):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        lg = rng.standard_normal((T, N)).astype(np.float32)
+    elif kind == "ties":
+        lg = rng.integers(-3, 4, (T, N)).astype(np.float32)
+        lg[rng.random((T, N)) < 0.3] = -0.0
+    else:  # "sparse": most columns unscored
+        lg = rng.standard_normal((T, N)).astype(np.float32)
+        lg[rng.random((T, N)) < 0.97] = -np.inf
+    lg[rng.random((T, N)) < 0.1] = -np.inf
+    return lg
+
+
+@pytest.mark.parametrize("T,N,k", [(4, 300, 16), (3, 65536, 512), (2, 131072, 2048), (5, 700, 900)])
+@pytest.mark.parametrize("kind", ["normal", "ties", "sparse"])
+def test_topk_exact(T, N, k, kind):
+    dev = _dev()
+    lg = _topk_logits(T, N, seed=N + k, kind=kind)
+    got = spa.sparse_attn_indexer_topk(torch.from_numpy(lg).to(dev), k).cpu().numpy()
+    want = oi.topk_entries(lg.astype(np.float64), k)
+    assert np.array_equal(got, want)
+
+
+def test_topk_candidate_ids():
+    dev = _dev()
+    rng = np.random.default_rng(30)
+    lg = _topk_logits(6, 16384, seed=31, kind="ties")
+    cand = np.stack([rng.permutation(131072)[:16384] for _ in range(6)]).astype(np.int32)
+    got = spa.sparse_attn_indexer_topk(torch.from_numpy(lg).to(dev), 512,
+                                       cand=torch.from_numpy(cand).to(dev)).cpu().numpy()
+    assert np.array_equal(got, oi.topk_entries(lg.astype(np.float64), 512, cand=cand))
