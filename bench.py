@@ -20,10 +20,8 @@ from __future__ import annotations
 
 import argparse
 import re
-import glob
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

@@ -1,6 +1,5 @@
 """Adapters from a seeded workload to the oracle's plain-numpy arguments (test helper)."""
 import numpy as np
-import torch
 
 import oracle
 from workloads import Workload, bf16_bits

@@ -5,7 +5,6 @@ or a hand-worked fixture fixes.  They look the oracle's functions up at call tim
 ``test_oracle_mutations.py`` can plant a mistake in the oracle and show that some pin catches it.
 """
 import json
-import math
 import os
 
 import numpy as np

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import sparse_paged_attention_gb300 as spa
-from oracle_io import oracle_args, oracle_columns, run_oracle
+from oracle_io import oracle_columns, run_oracle
 from workloads import build, make
 
 pytestmark = pytest.mark.gpu

@@ -5,7 +5,6 @@ code nearest to it (the decoder, itself pinned by tests/golden/e4m3_codes.json, 
 value), ties going to the code with the even mantissa, magnitudes past 448 saturating.
 """
 import numpy as np
-import pytest
 
 import oracle
 from oracle import kv_write as okw
