@@ -156,3 +156,32 @@ def test_topk_host_validation(lib, no_device):
     assert f(0x1000, 2, 10, None, 4, None, None) == S["SPA_ERR_NULL"]
     assert f(0x1002, 2, 10, None, 4, 0x2000, None) == S["SPA_ERR_ALIGN"]
     assert f(0x1000, 2, 10, 0x3001, 4, 0x2000, None) == S["SPA_ERR_ALIGN"]
+
+
+def test_header_is_plain_c_and_every_entry_point_links(lib, tmp_path):
+    """A C99 program that includes the header, takes the address of every declared entry point
+    and links against the library builds and runs (it calls only the version query)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "sparse_attn_paged.h"\n#include <stdio.h>\n'
+        "typedef void (*fn)(void);\n"
+        "int main(void) {\n"
+        "  const fn all[] = {\n" + "".join(f"    (fn){n},\n" for n in names) + "  };\n"
+        '  printf("%d %s\\n", (int)(sizeof all / sizeof all[0]), sparse_attn_paged_version());\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(spa.library_path())
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-lspa_gb300", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    n, version = out.stdout.split(" ", 1)
+    assert int(n) == len(names) and "sm_103a" in version
