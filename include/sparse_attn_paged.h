@@ -249,8 +249,9 @@ int sparse_attn_indexer_logits(const void* q, const float* weights, int32_t num_
  * Top-k selection over indexer logits (the step after sparse_attn_indexer_logits; FreeToken PR 634
  * lists a top-k test beside the logits kernel).  For each query t: the k entries with the largest
  * finite logits[t][c], in decreasing order of logit, ties going to the smaller entry index; -1
- * fills the row when fewer than k logits are finite (-inf and NaN are "not scored").  Column c is
- * entry c, or cand[t][c] when cand is given (as for the logits).  -0 and +0 are equal logits.
+ * fills the row when fewer than k logits are finite (infinities and NaN are "not scored").
+ * Column c is entry c, or cand[t][c] when cand is given (as for the logits).  -0 and +0 are
+ * equal logits.
  *   logits:   device fp32 [num_tokens][num_cols]; cand: device int32 [num_tokens][num_cols] or
  *             NULL; topk_idx: device int32 [num_tokens][k], the attention's top-k list.
  *   k:        0 .. 2048 (SPA_ERR_UNSUPPORTED above).

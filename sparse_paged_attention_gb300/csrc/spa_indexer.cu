@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include "spa_indexer.h"
+#include "spa_indexer_math.cuh"
 
 namespace spa {
 
@@ -37,24 +38,6 @@ constexpr int kPosOff = kWOff + kIdxMaxQ * kIdxHeads * 4;  // positions [8], seq
 constexpr int kBarOff = kPosOff + 2 * kIdxMaxQ * 4;        // mbarrier (8 B), tmem base, abort
 constexpr int kSmemUsed = kBarOff + 64;
 constexpr uint32_t kTmemCols = 256;
-
-// e2m1 code (4 bits) times a scale -> bf16 bits.  The magnitude is built from the code's fields
-// ((1 + m/2) 2^(e-1), or m/2 for e = 0), the product with a power of two is exact in fp32 (down to
-// fp32 subnormals; past the fp32 range it is inf), and the bf16 conversion of an exact value with
-// two significant bits is exact.  Bit 3 is the sign.
-__device__ __forceinline__ uint32_t e2m1_to_bf16_bits(uint32_t c, float scale) {
-  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-  const uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
-  const float v = __uint_as_float(mag) * scale;
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) | ((c & 8u) << 12);
-}
-
-// ue8m0 scale byte -> fp32: 2^(s - 127); 0 is the fp32 subnormal 2^-127; 0xFF is NaN.
-__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
-  if (s == 0u) return __uint_as_float(0x00400000u);
-  if (s == 255u) return __uint_as_float(0x7FC00000u);
-  return __uint_as_float(s << 23);
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

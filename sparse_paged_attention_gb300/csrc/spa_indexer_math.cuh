@@ -1,0 +1,68 @@
+// spa_indexer_math.cuh - the element arithmetic of the indexer kernels, callable on the host too
+// so that the very code the kernels run can be checked on a CPU against the oracle.
+//
+//   e2m1_to_bf16_bits / e8m0_to_f32: the fp4_e8m0_b32 key-row decoding (OCP MX E2M1 codes, E8M0
+//   scales), every product exact in bf16 (FreeToken PR 634, "Correctness and tests").
+//   topk_order_key: the 64-bit key whose order is the top-k output order.
+#pragma once
+
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_bf16.h>
+
+namespace spa {
+
+__host__ __device__ __forceinline__ float f32_from_bits(uint32_t u) {
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(u);
+#else
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+#endif
+}
+
+__host__ __device__ __forceinline__ uint32_t f32_bits(float f) {
+#ifdef __CUDA_ARCH__
+  return __float_as_uint(f);
+#else
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return u;
+#endif
+}
+
+// e2m1 code (4 bits) times a scale -> bf16 bits.  The magnitude is built from the code's fields
+// ((1 + m/2) 2^(e-1), or m/2 for e = 0), the product with a power of two is exact in fp32 (down to
+// fp32 subnormals; past the fp32 range it is inf), and the bf16 conversion of an exact value with
+// two significant bits is exact.  Bit 3 is the sign.
+__host__ __device__ __forceinline__ uint32_t e2m1_to_bf16_bits(uint32_t c, float scale) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = e ? (((e + 126u) << 23) | (m << 22)) : (m ? 0x3F000000u : 0u);
+  const float v = f32_from_bits(mag) * scale;
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) | ((c & 8u) << 12);
+}
+
+// ue8m0 scale byte -> fp32: 2^(s - 127); 0 is the fp32 subnormal 2^-127; 0xFF is NaN.
+__host__ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  if (s == 0u) return f32_from_bits(0x00400000u);
+  if (s == 255u) return f32_from_bits(0x7FC00000u);
+  return f32_from_bits(s << 23);
+}
+
+// Top-k order key of a scored logit (finite: -inf means "no entry"; +inf and NaN are not
+// scored either): the logit's order-preserving 32 bits (-0 folded into +0) above the complement
+// of the entry index, so that a larger key is a larger logit, or the same logit and a smaller
+// index.
+__host__ __device__ __forceinline__ bool topk_order_key(float x, uint32_t id,
+                                                        unsigned long long& key) {
+  if (!(x > -INFINITY && x < INFINITY)) return false;  // also false for NaN
+  if (x == 0.f) x = 0.f;
+  const uint32_t u = f32_bits(x);
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  key = ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - id);
+  return true;
+}
+
+}  // namespace spa

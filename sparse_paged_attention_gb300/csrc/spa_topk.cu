@@ -12,21 +12,13 @@
 // the k keys in order.  Each pass re-reads the logits row (from L2 for the sizes the indexer
 // writes); no pass waits on anything but __syncthreads.
 #include "spa_indexer.h"
+#include "spa_indexer_math.cuh"
 
 namespace spa {
 
 namespace {
 
 constexpr int kThreads = 512;
-
-__device__ __forceinline__ bool scored_key(float x, uint32_t id, unsigned long long& key) {
-  if (!(x > -INFINITY) || x != x) return false;  // -inf (no entry) and NaN are not scored
-  if (x == 0.f) x = 0.f;                          // -0 and +0 are the same logit
-  const uint32_t u = __float_as_uint(x);
-  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  key = ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - id);
-  return true;
-}
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   __shared__ unsigned int s_hist[256];
@@ -44,7 +36,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   unsigned int mine = 0;
   for (int c = tid; c < a.ncols; c += kThreads) {
     unsigned long long key;
-    mine += scored_key(__ldg(row + c), entry_of(c), key) ? 1u : 0u;
+    mine += topk_order_key(__ldg(row + c), entry_of(c), key) ? 1u : 0u;
   }
   atomicAdd(&s_count, mine);
   __syncthreads();
@@ -63,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       __syncthreads();
       for (int c = tid; c < a.ncols; c += kThreads) {
         unsigned long long key;
-        if (!scored_key(__ldg(row + c), entry_of(c), key)) continue;
+        if (!topk_order_key(__ldg(row + c), entry_of(c), key)) continue;
         if (shift < 64 && (key >> shift) != (prefix >> shift)) continue;
         atomicAdd(&s_hist[(key >> sh) & 0xFFu], 1u);
       }
@@ -113,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   __syncthreads();
   for (int c = tid; c < a.ncols; c += kThreads) {
     unsigned long long key;
-    if (!scored_key(__ldg(row + c), entry_of(c), key)) continue;
+    if (!topk_order_key(__ldg(row + c), entry_of(c), key)) continue;
     bool keep = true;
     if (shift < 64) {
       const unsigned long long kt = key >> shift, pt = prefix >> shift;
