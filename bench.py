@@ -628,7 +628,6 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np  # noqa: F401
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from oracle_io import oracle_args
     import oracle
@@ -647,12 +646,12 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) rows, random block tables and top-k; no dataset)",
-        "config": {"workload": "decode B=1 at position 32767, 64 heads, head_dim 512, window 128, "
-                               "top-k 512 of 8192 (ratio 4), page size 64, bf16 pools"},
+        "config": {"workload": describe(args.workload),
+                   "parallelism": "rank 0 only, host cores"},
         "impl": "reference",
         "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": os.cpu_count(),
                          "kind": "oracle",
-                         "sample": f"{args.steps} full decode calls, float64 numpy oracle"},
+                         "sample": f"{args.steps} full calls of the workload, float64 numpy oracle"},
         "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

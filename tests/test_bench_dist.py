@@ -42,3 +42,32 @@ def test_max_over_two_ranks():
 def test_single_rank_needs_no_process_group():
     assert bench.init_dist(1, "gloo") is None
     assert bench.max_over_ranks(None, 3.5) == 3.5
+
+
+def test_reference_arm_prints_the_contract_line():
+    """``bench.py --impl reference`` (the float64 oracle on the host cores) prints one JSON line
+    with the keys the driver reads."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, env={**os.environ, "RANK": "0", "WORLD_SIZE": "1"})
+    assert p.returncode == 0, p.stderr[-2000:]
+    line = json.loads(p.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["higher_is_better"] is False
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"] and "workload" in line["config"]
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=120, env={**os.environ, "RANK": "1", "WORLD_SIZE": "2"})
+    assert p.returncode == 0 and p.stdout.strip() == ""
