@@ -148,7 +148,8 @@ int validate(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const 
     return SPA_ERR_SHAPE;
   if (!std::isfinite(pr->scale)) return SPA_ERR_SHAPE;
   if (pr->head_dim % 64 != 0 || pr->head_dim > 512) return SPA_ERR_UNSUPPORTED;
-  if (pr->window + pr->topk > spa::kMaxColumns) return SPA_ERR_UNSUPPORTED;
+  // (the sum in 64 bits: two large int32 sizes must not wrap past the limit)
+  if ((long long)pr->window + (long long)pr->topk > spa::kMaxColumns) return SPA_ERR_UNSUPPORTED;
   if (pr->num_tokens == 0) return SPA_OK;
   if (!q || !out || !pr->positions) return SPA_ERR_NULL;
   if (pr->topk > 0 && !pr->topk_idx) return SPA_ERR_NULL;
@@ -428,6 +429,8 @@ int sparse_attn_paged_resolve_columns(const spa_pool_t* win, const spa_pool_t* c
   if (prob->num_tokens < 0 || prob->num_seqs < 1 || prob->window < 0 || prob->topk < 0 ||
       prob->ratio < 0)
     return SPA_ERR_SHAPE;
+  // (the column count in 64 bits: window + topk must not wrap)
+  if ((long long)prob->window + (long long)prob->topk > 0x7fffffffLL) return SPA_ERR_UNSUPPORTED;
   if (prob->num_tokens == 0 || prob->window + prob->topk == 0) return SPA_OK;
   if (!cols || !prob->positions) return SPA_ERR_NULL;
   if (prob->topk > 0 && !prob->topk_idx) return SPA_ERR_NULL;
