@@ -42,6 +42,11 @@
  *
  * Supported shapes: head_dim in {64, 128, ..., 512} (multiple of 64), num_heads >= 1 (heads
  * are processed in groups of 64), window + topk <= 1024, num_blocks * page_size <= 2^30.
+ *
+ * Per-device state: on its first call on a device the library sets its kernels' launch attributes
+ * and caches the SM count, cluster occupancy and the device address of its scratch array, for the
+ * rest of the process.  cudaDeviceReset() discards the attributes and the array but not the
+ * cache, so the library must not be used on a device after that device was reset.
  */
 #ifndef SPARSE_ATTN_PAGED_H
 #define SPARSE_ATTN_PAGED_H
@@ -135,9 +140,10 @@ int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa
  * exits) instead of a caller workspace.
  *   - The first call on a device, with that device current, looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture on that device.
- *   - Problems whose partials need more than SPA_NOALLOC_SCRATCH_BYTES (fp32 [T][S][H][D]
- *     partials plus [T][S][H] log-sum-exps, S splits per query) are rejected with
- *     SPA_ERR_WORKSPACE.
+ *   - The partials take fp32 [T][S][H][D] plus [T][S][H] log-sum-exps for S splits per query.  S
+ *     follows the SM count (about one split item per SM), and is lowered, down to 1, until the
+ *     partials fit in SPA_NOALLOC_SCRATCH_BYTES.  Only a problem whose single-split partials do not
+ *     fit (more than 127 tokens of 64 heads x head_dim 512) is rejected with SPA_ERR_WORKSPACE.
  *   - Every call on a device shares the one array and leaves its partials there: two calls that
  *     can overlap on the GPU (different streams without ordering between them) race and give
  *     wrong results.  Calls ordered on one stream are safe.

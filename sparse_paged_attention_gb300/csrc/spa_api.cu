@@ -9,6 +9,7 @@
 #include "sparse_attn_paged.h"
 #include "spa_indexer.h"
 #include "spa_launch.h"
+#include "spa_plan.h"
 
 namespace {
 
@@ -208,7 +209,8 @@ struct DecodePlan {
   int gh;                     // heads per group (64, or 32 to give one query more CTAs)
 };
 
-void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols);
+void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols,
+                    size_t cap_bytes = SIZE_MAX);
 
 DecodePlan decode_plan(const spa_problem_t* pr, int dev, int sms) {
   const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
@@ -237,31 +239,15 @@ DecodePlan decode_plan(const spa_problem_t* pr, int dev, int sms) {
   return pl;
 }
 
-// Split plan of the workspace path: enough splits to give every SM one item, at least 32
-// columns per split.
-void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols) {
-  const int C = pr->window + pr->topk > 0 ? pr->window + pr->topk : 1;
-  const long long groups = (pr->num_heads + 63) / 64;
-  const long long base = (long long)pr->num_tokens * groups;
-  long long want = base > 0 ? sms / base : 1;
-  if (want < 1) want = 1;
-  int c = (int)((C + want - 1) / want);
-  c = ((c + 31) / 32) * 32;
-  if (c > C) c = C;
-  int n = (C + c - 1) / c;
-  if (n > spa::merge_max_splits()) {  // the merge reads at most this many partials per head
-    c = (C + spa::merge_max_splits() - 1) / spa::merge_max_splits();
-    n = (C + c - 1) / c;
-  }
-  *cols = c;
-  *splits = n;
+// Split plan of the workspace path (spa_plan.h): enough splits to give every SM one item, at least
+// 32 columns per split, partials of at most cap_bytes.
+void decode_plan_ws(const spa_problem_t* pr, int sms, int* splits, int* cols, size_t cap_bytes) {
+  spa::plan_partials(pr->window + pr->topk, pr->num_tokens, pr->num_heads, pr->head_dim, sms,
+                     spa::merge_max_splits(), cap_bytes, splits, cols);
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 size_t workspace_bytes(const spa_problem_t* pr, int splits) {
-  const size_t tsh = (size_t)pr->num_tokens * splits * pr->num_heads;
-  return align256(tsh * pr->head_dim * sizeof(float)) + align256(tsh * sizeof(float));
+  return spa::partials_bytes(pr->num_tokens, pr->num_heads, pr->head_dim, splits);
 }
 
 int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_problem_t* pr,
@@ -288,10 +274,10 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
   bool merge = false;
   if (decode) {
     DecodePlan pl = decode_plan(pr, dev, sms);
-    if (force_partials && (pl.cluster > 1 || pl.splits == 1)) {
+    if (force_partials) {   // partials in the caller's buffer, as many splits as fit in it
       pl.cluster = 0;
       pl.gh = 64;
-      decode_plan_ws(pr, sms, &pl.splits, &pl.cols);
+      decode_plan_ws(pr, sms, &pl.splits, &pl.cols, ws_bytes);
     }
     p.gh = pl.gh;
     p.n_groups = (pr->num_heads + pl.gh - 1) / pl.gh;
@@ -306,7 +292,7 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
       const size_t tsh = (size_t)pr->num_tokens * pl.splits * pr->num_heads;
       p.ws_o = static_cast<float*>(ws);
       p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                          align256(tsh * pr->head_dim * sizeof(float)));
+                                          spa::plan_align256(tsh * pr->head_dim * sizeof(float)));
       p.decode = 1;
       merge = true;
     }
@@ -339,12 +325,12 @@ int run(const void* q, const spa_pool_t* win, const spa_pool_t* cmp, const spa_p
 }  // namespace
 
 namespace spa {
-size_t decode_partials_bytes(const spa_problem_t* prob) {
+size_t decode_partials_bytes(const spa_problem_t* prob, size_t cap_bytes) {
   if (!prob || prob->num_tokens < 0 || prob->num_heads < 1 || prob->head_dim < 1) return 0;
   int dev = 0, sms = 0;
   if (current_device(&dev, &sms) != SPA_OK) return 0;
   int splits = 1, cols = 1;
-  decode_plan_ws(prob, sms, &splits, &cols);
+  decode_plan_ws(prob, sms, &splits, &cols, cap_bytes);
   return workspace_bytes(prob, splits);
 }
 

@@ -91,8 +91,10 @@ cudaError_t prepare_attn_kernels();   // per-device one-time attributes (dynamic
 cudaError_t read_and_clear_error_word(int* value);
 
 // Decode through split-K partials in a caller-given buffer and the merge kernel, whatever the
-// usual plan would be (the path of the no-alloc entry point), and the bytes it needs.
-size_t decode_partials_bytes(const spa_problem_t* prob);
+// usual plan would be (the path of the no-alloc entry point), and the bytes its partials take when
+// the buffer holds cap_bytes (the split count shrinks until they fit; with one split they may
+// still not fit, which the caller checks).
+size_t decode_partials_bytes(const spa_problem_t* prob, size_t cap_bytes);
 int decode_with_partials(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
                          const spa_problem_t* prob, void* out, void* ws, size_t ws_bytes,
                          void* stream);

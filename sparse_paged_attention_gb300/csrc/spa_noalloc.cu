@@ -46,8 +46,9 @@ extern "C" int sparse_attn_paged_decode_noalloc(const void* q, const spa_pool_t*
                                                 const spa_pool_t* cmp, const spa_problem_t* prob,
                                                 void* out, void* stream) {
   if (!prob) return SPA_ERR_NULL;
-  // The partials of this problem must fit the built-in array; no larger buffer can be had here.
-  if (spa::decode_partials_bytes(prob) > kScratchBytes) return SPA_ERR_WORKSPACE;
+  // The partials of this problem must fit the built-in array (with as few as one split); no
+  // larger buffer can be had here.
+  if (spa::decode_partials_bytes(prob, kScratchBytes) > kScratchBytes) return SPA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);
   if (st != SPA_OK) return st;

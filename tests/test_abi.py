@@ -91,6 +91,12 @@ def test_host_validation(lib, no_device):
         assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_UNSUPPORTED"]
     _, _, pr, *_ = _args(W=600, K=600)
     assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_UNSUPPORTED"]
+    # window + top-k past the int32 range must not wrap below the column limit
+    _, _, pr, *_ = _args(W=2**31 - 1, K=2)
+    assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_UNSUPPORTED"]
+    assert lib.sparse_attn_paged_resolve_columns(ctypes.byref(pool), ctypes.byref(cpool),
+                                                 ctypes.byref(pr), 0x8000, None) == \
+        S["SPA_ERR_UNSUPPORTED"]
     _, _, pr, *_ = _args(W=-1)
     assert _prefill(lib, pool, cpool, pr, q, out) == S["SPA_ERR_SHAPE"]
     _, _, pr, *_ = _args(T=0)
