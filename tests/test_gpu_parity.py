@@ -102,7 +102,8 @@ def test_tiny_prefill_and_decode():
     check_no_device_error()
 
 
-@pytest.mark.parametrize("name", ["decode_b1_r4", "decode_b8_r128", "decode_b8_r4", "decode_b8_r0"])
+@pytest.mark.parametrize("name", ["decode_b1_r4", "decode_b8_r128", "decode_b8_r4", "decode_b8_r0",
+                                  "decode_b1_r128", "decode_b1_r0"])
 def test_decode_workloads(name):
     d = OnDevice(make(name), _dev())
     ref, _, _, _ = run_oracle(d.w)
@@ -123,12 +124,47 @@ def test_prefill_s8192_sampled():
     d = OnDevice(make("prefill_s8192_r4"), _dev())
     out = d.prefill()
     check_no_device_error()
+    check_convex_bound(out, d.w)
     toks = _sample_tokens(d.w.num_tokens, 50, 1)
     ref, _, _, _ = run_oracle(d.w, tokens=toks)
     compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_BF16, what="prefill S8192 (sampled)")
     # query 0 sees one column (token 0): its output is that V row rounded to bf16
     v0 = d.w.win.kv[int(d.w.win.block_table[0, 0]), 0, 1]
     assert torch.equal(out[0].cpu(), v0.expand(d.w.num_heads, -1))
+
+
+def check_convex_bound(out, w):
+    """Every output is a convex combination of V rows: |out| <= max |V| over the referenced rows
+    (bf16 rounding of the output adds at most 2^-8 of that), at every query and head."""
+    vals = []
+    for pool in (w.win, w.cmp):
+        if pool is None:
+            continue
+        if w.fp8:   # e4m3 code value times the row's V scale
+            nb, ps = pool.kv.shape[0], pool.kv.shape[1]
+            v = pool.kv[:, :, 1].contiguous().view(torch.float8_e4m3fn).float() * \
+                pool.v_scale.view(nb, ps, 1)
+        else:
+            v = pool.kv[:, :, 1].float()
+        vals.append(v[torch.isfinite(v)].abs().max())
+    vmax = float(max(vals)) * (1 + 2.0 ** -8)
+    o = out.float()
+    assert bool(torch.isfinite(o).all()), "non-finite output"
+    assert float(o.abs().max()) <= vmax, (float(o.abs().max()), vmax)
+
+
+@pytest.mark.parametrize("name", ["prefill_s8192_r128", "prefill_s8192_r0",
+                                  "prefill_s4096at28672_r4", "prefill_s2048_r4"])
+def test_benched_prefill_sampled(name):
+    """The other prefill shapes the bench times, at full size in the bench's launch configuration:
+    sampled queries against the oracle, every output against the convexity bound."""
+    d = OnDevice(make(name), _dev())
+    out = d.prefill()
+    check_no_device_error()
+    check_convex_bound(out, d.w)
+    toks = _sample_tokens(d.w.num_tokens, 40, 3)
+    ref, _, _, _ = run_oracle(d.w, tokens=toks)
+    compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_BF16, what=f"{name} (sampled)")
 
 
 def test_prefill_window_only_sampled():
@@ -253,6 +289,7 @@ def test_fp8_prefill_chunk_sampled():
     d = OnDevice(make("prefill_fp8_s4096_r4"), _dev())
     out = d.prefill()
     check_no_device_error()
+    check_convex_bound(out, d.w)
     toks = _sample_tokens(d.w.num_tokens, 40, 2)
     ref, _, _, _ = run_oracle(d.w, tokens=toks)
     compare(out, ref, tokens=toks, gate=REL_MEAN_GATE_FP8, what="fp8 prefill chunk (sampled)")

@@ -1,10 +1,11 @@
-"""The decode entry point that allocates nothing, against the ordinary decode entry point.
+"""The decode entry point that allocates nothing, against the ordinary decode entry point and
+against the float64 oracle.
 
-Some callers cannot call cudaMalloc where they decode (their allocator belongs to another runtime,
-or the decode step is being recorded into a CUDA graph that may hold no allocation).  For them
+Some callers cannot call cudaMalloc where they decode (their device allocator belongs to another
+runtime, or their host has no allocator hooks at that point).  For them
 sparse_attn_paged_decode_noalloc keeps the split-K partials in a scratch array built into the
-library.  This file is collected last so that a run stopping at the first failure has already run
-every other test.
+library and merges them with the separate merge kernel.  This file is collected last so that a run
+stopping at the first failure has already run every other test.
 """
 import ctypes
 
@@ -13,7 +14,8 @@ import pytest
 import torch
 
 import sparse_paged_attention_gb300 as spa
-from workloads import make
+from oracle_io import run_oracle
+from workloads import build, make
 
 pytestmark = pytest.mark.gpu
 
@@ -46,22 +48,51 @@ def _on_device(name):
             "cmp": None if w.cmp is None else spa.PagedPool(g(w.cmp.kv), g(w.cmp.block_table))}
 
 
-@pytest.mark.parametrize("name", ["decode_b8_r4", "decode_b1_r4", "tiny_r4"])
-def test_noalloc_matches_decode_twice(name):
+def _within(out, ref, what):
+    err = np.abs(out.float().cpu().numpy().astype(np.float64) - ref)
+    assert np.all(np.isfinite(err)), what
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (what, err.max(), err.mean())
+
+
+@pytest.mark.parametrize("name", ["decode_b8_r4", "decode_b8_r128", "decode_b8_r0",
+                                  "decode_b1_r4", "tiny_r4"])
+def test_noalloc_matches_decode_and_oracle_twice(name):
     d = _on_device(name)
     lib = spa.load_library()
     w = d["w"]
     ref = spa.sparse_attn_paged_decode(d["q"], d["win"], d["cmp"], d["tk"], d["pos"],
                                        window=w.window, ratio=w.ratio, scale=w.scale,
                                        seq_of_token=d["sot"])
-    ref_np = ref.float().cpu().numpy()
-    for _ in range(2):                      # the shared scratch keeps the previous call's partials
+    ref_np = ref.float().cpu().numpy().astype(np.float64)
+    exact, _, _, _ = run_oracle(w)          # the float64 definition itself
+    for call in range(2):                   # the shared scratch keeps the previous call's partials
         out = torch.full_like(d["q"], float("nan"))
         assert _call_noalloc_c(lib, d, out) == 0
         assert spa.sparse_attn_paged_check_errors() == 0
-        err = np.abs(out.float().cpu().numpy() - ref_np)
-        assert np.all(np.isfinite(err))
-        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+        _within(out, ref_np, f"{name} call {call}: against sparse_attn_paged_decode")
+        _within(out, exact, f"{name} call {call}: against the oracle")
+
+
+def test_noalloc_lowers_its_split_count_to_fit():
+    """32 decode queries of 64 heads x 512 over 640 columns: on 152 SMs the split plan would take
+    4 splits, whose partials (16.8 MB) exceed the built-in array; the entry point takes fewer,
+    longer splits instead of failing."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = build("decode_b32_r4_at1023", seq_positions=[np.array([1023])] * 32, num_heads=64,
+              head_dim=512, window=128, topk=512, ratio=4, page_size=64, decode=True, seed=7)
+    dev = torch.device("cuda:0")
+    g = lambda t: None if t is None else t.to(dev)
+    d = {"w": w, "q": g(w.q), "pos": g(w.positions), "sot": g(w.seq_of_token),
+         "tk": g(w.topk_idx), "win": spa.PagedPool(g(w.win.kv), g(w.win.block_table)),
+         "cmp": spa.PagedPool(g(w.cmp.kv), g(w.cmp.block_table))}
+    exact, _, _, _ = run_oracle(w)
+    lib = spa.load_library()
+    for call in range(2):
+        out = torch.full_like(d["q"], float("nan"))
+        assert _call_noalloc_c(lib, d, out) == 0
+        assert spa.sparse_attn_paged_check_errors() == 0
+        _within(out, exact, f"32 queries, call {call}: against the oracle")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
