@@ -1,28 +1,31 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 sparse paged attention hot path.
 
-Headline: one decode call of the B=1 workload at position 32767 (64 heads, head_dim 512, window 128,
-top-k 512 of 8192 compressed entries, ratio 4, page size 64; the shape of the FreeToken PR 633
-"Kernel time" table), in microseconds per call, L2 flushed between calls.  The same JSON line
-carries the other workloads of the table (decode B=8 at ratios 128/4/0, prefill S=8192, the e4m3
-prefill chunk), the paged KV write, the compressor's gated pool and the indexer logits at the
-pages' shapes, with their achieved GB/s or TFLOP/s against the measured GB300 peaks.
+Headline: one prefill call of 8192 queries from position 0 (64 heads, head_dim 512, window 128,
+top-k 512 of the causally valid compressed entries, ratio 4, page size 64; the "sparse prefill r4
+S8192" shape of the FreeToken PR 633 "Kernel time" table), in microseconds per call, L2 flushed
+before every call.  The same JSON line carries the other four configurations (the tiny case, decode
+B=1, decode B=8 at ratios 128/4/0, the e4m3 prefill chunk) with their achieved GB/s or TFLOP/s
+against the measured GB300 peaks.  The remaining shapes of the pages' tables (the other decode and
+prefill shapes, the paged KV write, the compressor's gated pool, the indexer logits and top-k) are
+printed on one more JSON line, to stderr, before it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload NAME] [--no-sub | --sub NAME,...] [--no-cpu-baseline]
+                    [--workload NAME] [--headline-only] [--sub NAME,...] [--no-cpu-baseline]
 
-For N > 1 (torchrun, one rank per GPU) every rank runs the same workload on its own GPU (the
-problem shards into independent queries/sequences; there is no data-path collective): the
-reported time is the maximum over ranks and scaling is weak.  ``--impl reference`` times the
-float64 CPU oracle on the host cores instead (rank 0 only).
+For N > 1 (torchrun, one rank per GPU) the job is a batch of N independent copies of the workload's
+sequences (N prefill sequences, or 8N decode sequences for the B=8 shapes), partitioned by
+sequence: rank r holds and computes shard r only, with no data-path collective (a barrier and a
+max over ranks time the job).  Scaling is weak.  ``--impl reference`` times the float64 CPU oracle
+on the host cores instead (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
-import re
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -34,10 +37,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "sparse attn µs/call; decode HBM GB/s and prefill TFLOP/s as % of GB300 peak"
-HEADLINE = "decode_b1_r4"
-SUB_WORKLOADS = ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0", "prefill_s8192_r4",
-                 "prefill_fp8_s4096_r4", "decode_b1_r128", "decode_b1_r0", "prefill_s2048_r4",
-                 "prefill_s4096at28672_r4", "prefill_s8192_r128", "prefill_s8192_r0"]
+HEADLINE = "prefill_s8192_r4"
+# the five configurations: c1 tiny, c2 decode B=1, c3 decode B=8 (three ratios), c4 prefill
+# S=8192, c5 the e4m3 prefill chunk
+CONFIGS = {"c1": ["tiny_r4"], "c2": ["decode_b1_r4"],
+           "c3": ["decode_b8_r128", "decode_b8_r4", "decode_b8_r0"],
+           "c4": ["prefill_s8192_r4"], "c5": ["prefill_fp8_s4096_r4"]}
+OTHER_SHAPES = ["decode_b1_r128", "decode_b1_r0", "prefill_s2048_r4", "prefill_s4096at28672_r4",
+                "prefill_s8192_r128", "prefill_s8192_r0"]
 KV_WRITES = {"kv_write_fp8_t65536": True, "kv_write_t65536": False}   # name -> e4m3 pool
 GATED_POOLS = {"gated_pool_b%d_r%d_d%d" % s: s for s in
                [(b, r, d) for b in (1, 8) for r in (8, 128) for d in (128, 512)]}
@@ -58,7 +65,13 @@ INDEXERS = {
     "indexer_cand_decode_b1_ctx131072_nc16384": ("cand", 1, 131071, 1, 1, 16384),
     "indexer_cand_decode_b4_ctx131072_nc16384": ("cand", 1, 131071, 1, 4, 16384),
 }
+TOPK_SHAPES = {"topk_t1_n65536_k512": (1, 65536, 512), "topk_t128_n8192_k512": (128, 8192, 512),
+               "topk_t2048_n32768_k512": (2048, 32768, 512)}
 FLUSH_BYTES = 512 << 20   # > 129 MB of L2
+# a device-side wait enqueued before each timed call, so that the GPU is still busy with it while
+# the host enqueues the start event, the call and the end event: the events then bracket device
+# time only (about 100 us at GB300 clocks)
+SPIN_CYCLES = 200_000
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -92,6 +105,15 @@ def max_over_ranks(dist, value: float, device=None) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------------------------
 # accounting
 # ----------------------------------------------------------------------------------------------
@@ -117,6 +139,21 @@ def load_peaks():
             "measured"
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_of(w, us, peaks):
+    """Achieved rate of one call against its bound: decode HBM bytes against the copy peak,
+    prefill flops against the dense tensor peak of the kernel's operand type (bf16 measured
+    burst; e4m3 twice that, the nominal fp8/bf16 ratio), both for a kernel timed alone."""
+    work = algorithmic_work(w)
+    if w.decode or w.name == "tiny_r4":
+        gbs = work["bytes"] / (us * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s",
+                "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}, work
+    tf = work["flops"] / (us * 1e-6) / 1e12
+    peak = peaks["bf16_tflops"] * (2.0 if w.fp8 else 1.0)
+    return {"bound": "tensor", "achieved": round(tf, 1), "unit": "TFLOP/s", "peak": peak,
+            "frac": round(tf / peak, 4)}, work
 
 
 def _code_only(text: str) -> str:
@@ -176,7 +213,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -218,14 +255,15 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------------------------
 class Runner:
-    """One workload resident on the GPU plus the call that computes it through the C ABI."""
+    """One workload resident on the GPU plus the C-ABI call that computes it, its argument structs
+    built once (so a timed call is the library call and nothing else)."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, seed=0):
         import torch
         import sparse_paged_attention_gb300 as spa
         from workloads import make
         self.spa = spa
-        self.w = w = make(name)
+        self.w = w = make(name, seed=seed)
         g = lambda t: None if t is None else t.to(device)
         self.q, self.pos = g(w.q), g(w.positions)
         self.tk = g(w.topk_idx) if w.topk > 0 else None
@@ -235,29 +273,24 @@ class Runner:
         self.cmp = None if w.cmp is None else spa.PagedPool(
             g(w.cmp.kv), g(w.cmp.block_table), g(w.cmp.k_scale), g(w.cmp.v_scale))
         self.out = torch.empty_like(self.q)
-        self.kw = dict(window=w.window, ratio=w.ratio, scale=w.scale, seq_of_token=self.sot)
+        self.call = self.bind(self.q, self.tk, self.pos, self.out)
+        # a decode plan with a workspace adds the merge kernel; every other plan is one launch
+        self.launches_per_call = 2 if getattr(self.call, "workspace", None) is not None and \
+            self.call.workspace.numel() > 16 else 1
+
+    def bind(self, q, tk, pos, out):
+        w = self.w
+        kw = dict(window=w.window, ratio=w.ratio, scale=w.scale, seq_of_token=self.sot, out=out,
+                  fp8=w.fp8)
         if w.decode:
-            n = spa.sparse_attn_paged_decode_workspace_size(self.q, self.win, self.tk, self.pos,
-                                                            **self.kw)
-            self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
-            self.fn = spa.sparse_attn_paged_decode_fp8 if w.fp8 else spa.sparse_attn_paged_decode
-            # a plan that needs a workspace adds the merge kernel; the cluster plan is one launch
-            self.launches_per_call = 2 if n > 0 else 1
-        else:
-            self.ws = None
-            self.fn = spa.sparse_attn_paged_prefill_fp8 if w.fp8 else spa.sparse_attn_paged_prefill
-            self.launches_per_call = 1
-
-    def call(self, q=None, tk=None, pos=None, out=None):
-        kw = dict(self.kw, out=self.out if out is None else out)
-        if self.ws is not None:
-            kw["workspace"] = self.ws
-        return self.fn(self.q if q is None else q, self.win, self.cmp,
-                       self.tk if tk is None else tk, self.pos if pos is None else pos, **kw)
+            return self.spa.bind_decode(q, self.win, self.cmp, tk, pos, **kw)
+        return self.spa.bind_prefill(q, self.win, self.cmp, tk, pos, **kw)
 
 
-def time_device(fn, steps, warmup, flush, dist=None):
-    """Per-call device time (ms) of `steps` calls, L2 flushed before each (outside the events)."""
+def time_calls(fn, steps, warmup, flush, dist=None):
+    """Per-call device time (ms) of `steps` calls: L2 flushed before each, then a device-side
+    wait that keeps the GPU busy while the host enqueues the start event, the call and the end
+    event (outside the events), so each event pair brackets the call's device time."""
     import torch
     for _ in range(warmup):
         fn()
@@ -269,12 +302,19 @@ def time_device(fn, steps, warmup, flush, dist=None):
     torch.cuda.synchronize()
     for a, b in ev:
         flush.zero_()
+        torch.cuda._sleep(SPIN_CYCLES)
         a.record(stream)
         fn()
         b.record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def stats_us(times_ms):
+    us = [1e3 * t for t in times_ms]
+    return {"us": round(statistics.mean(us), 3), "us_median": round(statistics.median(us), 3),
+            "us_min": round(min(us), 3), "us_max": round(max(us), 3), "calls": len(us)}
 
 
 def time_graph(fn, reps=20, rounds=10):
@@ -307,9 +347,10 @@ def time_graph(fn, reps=20, rounds=10):
     return statistics.median(out)
 
 
-def time_e2e(r, steps, warmup, flush):
-    """The same call with host inputs: pinned host -> device copy of q, top-k and positions,
-    the call, device -> host copy of out, all inside the timed region."""
+def time_e2e(r, steps, warmup, flush, dist=None):
+    """The same call from host buffers: pinned host -> device copies of q, the top-k lists and
+    the positions, the library call, the device -> host copy of out, all inside the timed region
+    (the pools are the resident KV cache)."""
     import torch
     q_h = r.w.q.pin_memory()
     pos_h = r.w.positions.pin_memory()
@@ -317,22 +358,24 @@ def time_e2e(r, steps, warmup, flush):
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype, pin_memory=True)
     q_d, pos_d = torch.empty_like(r.q), torch.empty_like(r.pos)
     tk_d = torch.empty_like(r.tk) if r.tk is not None else None
+    out_d = torch.empty_like(r.out)
+    call = r.bind(q_d, tk_d, pos_d, out_d)
 
     def step():
         q_d.copy_(q_h, non_blocking=True)
         pos_d.copy_(pos_h, non_blocking=True)
         if tk_d is not None:
             tk_d.copy_(tk_h, non_blocking=True)
-        r.call(q=q_d, tk=tk_d, pos=pos_d)
-        out_h.copy_(r.out, non_blocking=True)
+        call()
+        out_h.copy_(out_d, non_blocking=True)
 
-    times = time_device(step, steps, warmup, flush)
+    times = time_calls(step, steps, warmup, flush, dist)
     h2d = q_h.numel() * 2 + pos_h.numel() * 4 + (tk_h.numel() * 4 if tk_h is not None else 0)
     d2h = out_h.numel() * 2
     return times, h2d, d2h
 
 
-def measure_workload(name, device, steps, warmup, flush, peaks):
+def measure_workload(name, device, steps, warmup, flush, peaks, graph=True):
     import torch
     r = Runner(name, device)
     r.call()
@@ -340,25 +383,15 @@ def measure_workload(name, device, steps, warmup, flush, peaks):
     st = r.spa.sparse_attn_paged_check_errors()
     if st:
         raise RuntimeError(f"{name}: device error word {st}")
-    times = time_device(r.call, steps, warmup, flush)
-    us = 1e3 * statistics.mean(times)
-    work = algorithmic_work(r.w)
-    d = {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
-         "calls": steps, "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"]}
-    try:
-        d["us_warm_graph"] = round(1e3 * time_graph(r.call, reps=20 if r.w.decode else 3), 3)
-    except Exception as e:  # noqa: BLE001 - reported, never fatal to the cold-L2 number
-        d["us_warm_graph"] = None
-        d["graph_error"] = str(e)[:200]
-    if r.w.decode:
-        gbs = work["bytes"] / (us * 1e-6) / 1e9
-        d.update(bound="hbm", achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm_gbs"],
-                 frac=round(gbs / peaks["hbm_gbs"], 4))
-    else:
-        tf = work["flops"] / (us * 1e-6) / 1e12
-        peak = peaks["bf16_tflops_sustained"] * (2.0 if r.w.fp8 else 1.0)
-        d.update(bound="tensor", achieved=round(tf, 1), unit="TFLOP/s", peak=peak,
-                 frac=round(tf / peak, 4), frac_of_bf16_peak=round(tf / peaks["bf16_tflops"], 4))
+    s = stats_us(time_calls(r.call, steps, warmup, flush))
+    roof, _ = roofline_of(r.w, s["us"], peaks)
+    d = dict(s, **roof)
+    if graph:
+        try:
+            d["us_warm_graph"] = round(1e3 * time_graph(r.call, reps=20 if r.w.decode else 3), 3)
+        except Exception as e:  # noqa: BLE001 - reported, never fatal to the cold-L2 number
+            d["us_warm_graph"] = None
+            d["graph_error"] = str(e)[:120]
     del r
     torch.cuda.empty_cache()
     return d
@@ -387,13 +420,11 @@ def measure_kv_write(name, device, steps, flush, peaks):
     call()
     if spa.sparse_attn_paged_check_errors():
         raise RuntimeError(f"{name}: device error word")
-    times = time_device(call, steps, 3, flush)
-    us = 1e3 * statistics.mean(times)
+    s = stats_us(time_calls(call, steps, 3, flush))
     nbytes = T * (4 * D + (2 * D + 8 if fp8 else 4 * D))
-    gbs = nbytes / (us * 1e-6) / 1e9
-    return {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
-            "calls": steps, "algorithmic_bytes": nbytes, "bound": "hbm", "achieved": round(gbs, 1),
-            "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    gbs = nbytes / (s["us"] * 1e-6) / 1e9
+    return dict(s, bound="hbm", achieved=round(gbs, 1), unit="GB/s", peak=peaks["hbm_gbs"],
+                frac=round(gbs / peaks["hbm_gbs"], 4))
 
 
 def measure_gated_pool(name, device, steps, flush, peaks):
@@ -408,15 +439,12 @@ def measure_gated_pool(name, device, steps, flush, peaks):
     out = torch.empty((B, D), dtype=torch.float32, device=device)
     call = lambda: spa.sparse_attn_gated_pool(kv, gate, out)
     call()
-    times = time_device(call, steps, 3, flush)
-    us = 1e3 * statistics.mean(times)
+    s = stats_us(time_calls(call, steps, 3, flush))
     warm = 1e3 * time_graph(call)
     nbytes = 8 * B * R * D + 4 * B * D
-    gbs = nbytes / (us * 1e-6) / 1e9
-    return {"us_per_call": round(us, 3), "us_median": round(1e3 * statistics.median(times), 3),
-            "warm_l2_graph_us": round(warm, 3), "calls": steps, "algorithmic_bytes": nbytes,
-            "bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s", "peak": peaks["hbm_gbs"],
-            "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    gbs = nbytes / (s["us"] * 1e-6) / 1e9
+    return dict(s, us_warm_graph=round(warm, 3), bound="hbm", achieved=round(gbs, 1), unit="GB/s",
+                peak=peaks["hbm_gbs"], frac=round(gbs / peaks["hbm_gbs"], 4))
 
 
 def measure_indexer(name, device, flush, peaks):
@@ -441,8 +469,7 @@ def measure_indexer(name, device, flush, peaks):
     if spa.sparse_attn_paged_check_errors():
         raise RuntimeError(f"{name}: device error word")
     big = n * x.num_cols >= (1 << 24)
-    times = time_device(call, 5 if big else 30, 3, flush)
-    us = 1e3 * statistics.mean(times)
+    s = stats_us(time_calls(call, 5 if big else 30, 3, flush))
     warm = 1e3 * time_graph(call, reps=3 if big else 20, rounds=5)
     p = x.positions.numpy().astype(np.int64)
     if x.cand is None:
@@ -454,12 +481,29 @@ def measure_indexer(name, device, flush, peaks):
         rows = int(scored.sum())
     flops = 2.0 * 32 * 128 * float(scored.sum())
     nbytes = 68 * rows + x.q.numel() * 2 + x.weights.numel() * 4 + out.numel() * 4
-    tf = flops / (us * 1e-6) / 1e12
-    gbs = nbytes / (us * 1e-6) / 1e9
-    return {"us_per_call": round(us, 3), "warm_l2_graph_us": round(warm, 3),
-            "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-            "tflops": round(tf, 2), "frac_bf16_tensor": round(tf / peaks["bf16_tflops"], 4),
-            "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    tf = flops / (s["us"] * 1e-6) / 1e12
+    gbs = nbytes / (s["us"] * 1e-6) / 1e9
+    return dict(s, us_warm_graph=round(warm, 3), tflops=round(tf, 2),
+                frac_bf16_tensor=round(tf / peaks["bf16_tflops"], 4), gbs=round(gbs, 1),
+                frac_hbm=round(gbs / peaks["hbm_gbs"], 4))
+
+
+def measure_topk(name, device, flush, peaks):
+    """Top-k selection over indexer logits (T rows of N fp32 logits, k entries kept): bytes = the
+    logits read once (the kernel's passes re-read them from L2) plus the int32 lists written."""
+    import numpy as np
+    import torch
+    import sparse_paged_attention_gb300 as spa
+    T, N, k = TOPK_SHAPES[name]
+    rng = np.random.default_rng(6)
+    lg = torch.from_numpy(rng.standard_normal((T, N)).astype(np.float32)).to(device)
+    out = torch.empty((T, k), dtype=torch.int32, device=device)
+    call = lambda: spa.sparse_attn_indexer_topk(lg, k, out=out)
+    call()
+    s = stats_us(time_calls(call, 30, 3, flush))
+    nbytes = T * N * 4 + T * k * 4
+    gbs = nbytes / (s["us"] * 1e-6) / 1e9
+    return dict(s, gbs=round(gbs, 1), frac_hbm=round(gbs / peaks["hbm_gbs"], 4))
 
 
 def cpu_baseline(name, seconds):
@@ -474,9 +518,20 @@ def cpu_baseline(name, seconds):
         return {"error": str(e)[:200]}
 
 
-def oracle_timing(name, seconds):
-    """Time the oracle on up to `seconds` of work for workload `name` (per call = all its
-    queries; prefill workloads are sampled query by query and scaled to a full call)."""
+def sample_args(a, toks):
+    """The oracle's arguments restricted to the queries `toks` (their q, positions, sequence ids
+    and top-k lists; the pools and block tables whole), so that its cost is that of those
+    queries alone."""
+    b = dict(a)
+    for k in ("q_bits", "positions", "seq_ids", "topk_idx"):
+        b[k] = a[k][toks]
+    return b
+
+
+def oracle_timing(name, seconds, max_queries=None):
+    """Time the oracle on about `seconds` of work for workload `name`: queries are drawn at random
+    in groups of up to 8 and the time per query is scaled to a full call of all the workload's
+    queries (a decode call of a few queries runs whole)."""
     import numpy as np
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from oracle_io import oracle_args
@@ -486,24 +541,32 @@ def oracle_timing(name, seconds):
     a = oracle_args(w)
     T = w.num_tokens
     rng = np.random.default_rng(0)
-    done, t0 = 0, time.perf_counter()
+    t0 = time.perf_counter()
     queries = 0
-    while time.perf_counter() - t0 < seconds:
-        toks = rng.choice(T, size=min(T, 8), replace=False) if T > 8 else None
-        oracle.sparse_paged_attention(**a, tokens=toks)
-        queries += T if toks is None else len(toks)
-        done += 1
+    while time.perf_counter() - t0 < seconds and (max_queries is None or queries < max_queries):
+        toks = np.sort(rng.choice(T, size=min(T, 8), replace=False))
+        oracle.sparse_paged_attention(**sample_args(a, toks))
+        queries += len(toks)
     el = time.perf_counter() - t0
     per_query = el / queries
     return {"us_per_call": per_query * T * 1e6, "queries": int(queries), "seconds": round(el, 2),
             "cores": os.cpu_count(), "per_call_queries": T}
 
 
+DESCRIBE = {
+    "prefill_s8192_r4": "prefill S=8192 from position 0, 64 heads, head_dim 512, window 128, "
+                        "top-k 512 of the causally valid compressed entries (ratio 4), page size "
+                        "64, bf16 pools",
+    "decode_b1_r4": "decode B=1 at position 32767, 64 heads, head_dim 512, window 128, top-k 512 "
+                    "of 8192 (ratio 4), page size 64, bf16 pools",
+    "prefill_fp8_s4096_r4": "e4m3 prefill chunk of 4096 queries at 28672..32767, 64 heads, "
+                            "head_dim 512, window 128, top-k 512 of 8192 (ratio 4), page size 64, "
+                            "e4m3 pools with per-row fp32 scales",
+}
+
+
 def describe(name):
-    if name == HEADLINE:
-        return ("decode B=1 at position 32767, 64 heads, head_dim 512, window 128, top-k 512 of "
-                "8192 (ratio 4), page size 64, bf16 pools")
-    return name
+    return DESCRIBE.get(name, name)
 
 
 def run_gpu(args):
@@ -518,54 +581,74 @@ def run_gpu(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     headline = args.workload
+    only = None if args.sub is None else set(args.sub.split(","))
+    keep = lambda name: only is None or name in only
     with ClockSampler(local) as clk:
-        r = Runner(headline, device)
-        times = time_device(r.call, args.steps, args.warmup, flush, dist)
+        # shard `rank` of a batch of `world` independent copies of the workload's sequences
+        r = Runner(headline, device, seed=rank)
+        r.call()
+        if spa.sparse_attn_paged_check_errors():
+            raise RuntimeError("device error word set by the first call")
+        times = time_calls(r.call, args.steps, args.warmup, flush, dist)
         st = spa.sparse_attn_paged_check_errors()
         if st:
             raise RuntimeError(f"device error word {st}")
-        us = 1e3 * statistics.mean(times)
-        us_max = max_over_ranks(dist, us, device)
-        warm_us = 1e3 * time_graph(r.call)
-        e2e_times, h2d, d2h = time_e2e(r, args.steps, args.warmup, flush)
+        head = stats_us(times)
+        us_job = max_over_ranks(dist, head["us"], device)
+        med_job = max_over_ranks(dist, head["us_median"], device)
+        max_job = max_over_ranks(dist, head["us_max"], device)
+        roof, work = roofline_of(r.w, us_job, peaks)
+        work_job = {k: sum_over_ranks(dist, float(v), device) for k, v in work.items()}
+        warm_us = 1e3 * time_graph(r.call, reps=20 if r.w.decode else 3)
+        e2e_times, h2d, d2h = time_e2e(r, args.steps, args.warmup, flush, dist)
         e2e_us = max_over_ranks(dist, 1e3 * statistics.mean(e2e_times), device)
         launches = r.launches_per_call * args.steps
-        work = algorithmic_work(r.w)
+        w_desc = r.w
         del r
-        sub = {}
-        only = None if args.sub is None else set(args.sub.split(","))
-        keep = lambda name: only is None or name in only
-        if not args.no_sub:
-            for name in SUB_WORKLOADS:
-                if name == headline or not keep(name):
-                    continue
+        torch.cuda.empty_cache()
+        configs, detail = {}, {}
+        if not args.headline_only:
+            for cid, names in CONFIGS.items():
+                for name in names:
+                    if name == headline or not keep(name):
+                        continue
+                    try:
+                        n = 50 if name.startswith("decode") or name == "tiny_r4" else 10
+                        configs[name] = dict(config=cid, **measure_workload(
+                            name, device, n, 3, flush, peaks))
+                    except Exception as e:  # noqa: BLE001 - reported, not fatal
+                        configs[name] = {"config": cid, "error": str(e)[:200]}
+            for name in filter(keep, OTHER_SHAPES):
                 try:
                     n = 50 if name.startswith("decode") else 10
-                    sub[name] = measure_workload(name, device, n, 3, flush, peaks)
-                except Exception as e:  # noqa: BLE001 - an unfinished path is reported, not fatal
-                    sub[name] = {"error": str(e)[:300]}
+                    detail[name] = measure_workload(name, device, n, 3, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - reported, not fatal
+                    detail[name] = {"error": str(e)[:200]}
             for name in filter(keep, KV_WRITES):
                 try:
-                    sub[name] = measure_kv_write(name, device, 50, flush, peaks)
+                    detail[name] = measure_kv_write(name, device, 50, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
-                    sub[name] = {"error": str(e)[:300]}
+                    detail[name] = {"error": str(e)[:200]}
             for name in filter(keep, GATED_POOLS):
                 try:
-                    sub[name] = measure_gated_pool(name, device, 50, flush, peaks)
+                    detail[name] = measure_gated_pool(name, device, 50, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
-                    sub[name] = {"error": str(e)[:300]}
-            # the indexer legs run only when named in --sub: its kernel has not yet been run
-            # to completion on a GPU
-            for name in (n for n in INDEXERS if only is not None and n in only):
+                    detail[name] = {"error": str(e)[:200]}
+            for name in filter(keep, INDEXERS):
                 try:
-                    sub[name] = measure_indexer(name, device, flush, peaks)
+                    detail[name] = measure_indexer(name, device, flush, peaks)
                 except Exception as e:  # noqa: BLE001 - reported, not fatal
-                    sub[name] = {"error": str(e)[:300]}
+                    detail[name] = {"error": str(e)[:200]}
+            for name in filter(keep, TOPK_SHAPES):
+                try:
+                    detail[name] = measure_topk(name, device, flush, peaks)
+                except Exception as e:  # noqa: BLE001 - reported, not fatal
+                    detail[name] = {"error": str(e)[:200]}
         # keep the GPU busy long enough for the clock sampler to see it under load
-        r = Runner(headline, device)
+        r = Runner(headline, device, seed=rank)
         t_end = time.time() + 1.0
         while time.time() < t_end:
-            for _ in range(200):
+            for _ in range(20):
                 r.call()
             torch.cuda.synchronize()
         del r
@@ -573,26 +656,26 @@ def run_gpu(args):
 
     if rank != 0:
         return
-    decode = headline.startswith("decode") or headline == "tiny_r4"
-    if decode:
-        achieved = work["bytes"] / (us_max * 1e-6) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        achieved = work["flops"] / (us_max * 1e-6) / 1e12
-        pk = peaks["bf16_tflops_sustained"] * (2.0 if "fp8" in headline else 1.0)
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
-                "frac": round(achieved / pk, 4)}
-    roof.update(traffic=ncu_traffic("attn_kernel", headline), peak_source=peak_src,
-                note="algorithmic work / device time of the whole call (all of its kernels)")
+    roof.update(kernel="attn_kernel", traffic=ncu_traffic("attn_kernel", headline),
+                peak_source=f"{peak_src} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops burst'})",
+                note="algorithmic work of one call / its device time (one launch of the "
+                     "attention kernel per call)")
+    if world > 1:
+        roof["note"] += "; all ranks' work over the slowest rank's time"
+        if roof["bound"] == "tensor":
+            roof["achieved"] = round(work_job["flops"] / (us_job * 1e-6) / 1e12, 1)
+        else:
+            roof["achieved"] = round(work_job["bytes"] / (us_job * 1e-6) / 1e9, 1)
+        roof["frac"] = round(roof["achieved"] / (roof["peak"] * world), 4)
+    seqs = w_desc.num_seqs
     line = {
         "metric": METRIC,
-        "value": round(us_max, 3),
+        "value": round(us_job, 3),
         "unit": "us/call",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(us_max / 1e3, 6),
+        "ms_per_step": round(us_job / 1e3, 6),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
@@ -600,47 +683,73 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,1) rows, random block tables and top-k; no dataset)",
         "config": {"workload": describe(headline),
                    "l2": f"flushed before every call ({FLUSH_BYTES >> 20} MiB write)",
-                   "parallelism": f"{world} independent replica(s), no collective"},
+                   "parallelism": (f"batch of {world} independent copies of the workload "
+                                   f"({world * seqs} sequences), one shard per rank by sequence, "
+                                   f"no collective" if world > 1 else "one GPU")},
+        "timing": {"us_median": round(med_job, 3), "us_max": round(max_job, 3),
+                   "us_min": head["us_min"], "calls": args.steps,
+                   "how": "CUDA events on the launching stream around each call; L2 flush and a "
+                          "device-side wait enqueued before the start event"},
         "roofline": roof,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
-        "warm_l2_graph": {"value": round(warm_us, 3), "unit": "us/call",
-                          "how": "20 calls captured in one CUDA graph, replayed with L2 warm; "
-                                 "median of 10 replays (the pages' measuring method)"},
+        "warm_l2_graph_us": round(warm_us, 3),
         "clocks": clocks,
-        "workloads": sub,
+        "configs": {k: {kk: v[kk] for kk in ("config", "us", "us_median", "us_max",
+                                             "us_warm_graph", "achieved", "unit", "frac", "error")
+                        if kk in v} for k, v in configs.items()},
     }
     if not args.no_cpu_baseline:
         cb = cpu_baseline(headline, args.cpu_seconds)
         if "us_per_call" in cb:
-            line["cpu_baseline"] = {"value": round(cb["us_per_call"], 1), "unit": "us/call",
-                                    "cores": cb["cores"], "kind": "oracle",
-                                    "sample": f"{cb['queries']} decode calls of the same workload "
-                                              f"in {cb['seconds']} s, float64 numpy, BLAS threads "
-                                              f"at the library default"}
+            line["cpu_baseline"] = {
+                "value": round(cb["us_per_call"], 1), "unit": "us/call", "cores": cb["cores"],
+                "kind": "oracle",
+                "sample": f"{cb['queries']} of the {cb['per_call_queries']} queries, drawn at "
+                          f"random, in {cb['seconds']} s (float64 numpy, BLAS threads at the "
+                          f"library default), scaled to a full call"}
         else:
             line["cpu_baseline"] = {"value": None, "kind": "oracle", "error": cb.get("error")}
+    if detail:
+        compact = {k: {kk: v[kk] for kk in ("us", "us_median", "us_warm_graph", "achieved", "unit",
+                                            "frac", "tflops", "gbs", "frac_hbm",
+                                            "frac_bf16_tensor", "error") if kk in v}
+                   for k, v in detail.items()}
+        print(json.dumps({"bench_detail": compact}), file=sys.stderr, flush=True)
     print(json.dumps(line), flush=True)
 
 
 def run_reference(args):
+    """The reference arm: the float64 oracle on the host cores, rank 0 only.  A full call of the
+    prefill workloads takes the oracle minutes, so each step is a bounded sample of the call's
+    queries (at most --ref-queries, drawn at random), timed and scaled to the full call."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    import numpy as np
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from oracle_io import oracle_args
     import oracle
     from workloads import make
     w = make(args.workload)
     a = oracle_args(w)
+    T = w.num_tokens
+    rng = np.random.default_rng(0)
+    nq = min(T, args.ref_queries)
+
+    def step():
+        toks = np.sort(rng.choice(T, size=nq, replace=False)) if nq < T else np.arange(T)
+        t0 = time.perf_counter()
+        oracle.sparse_paged_attention(**sample_args(a, toks))
+        return (time.perf_counter() - t0) * T / nq
+
     for _ in range(args.warmup):
-        oracle.sparse_paged_attention(**a)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.sparse_paged_attention(**a)
-    el = time.perf_counter() - t0
-    us = el / args.steps * 1e6
+        step()
+    per_call = [step() for _ in range(args.steps)]
+    us = statistics.mean(per_call) * 1e6
+    sample = (f"{nq} of the {T} queries per step, drawn at random, scaled to the full call"
+              if nq < T else "every query of the call")
     line = {
         "metric": METRIC, "value": round(us, 1), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 4),
@@ -650,8 +759,7 @@ def run_reference(args):
                    "parallelism": "rank 0 only, host cores"},
         "impl": "reference",
         "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": os.cpu_count(),
-                         "kind": "oracle",
-                         "sample": f"{args.steps} full calls of the workload, float64 numpy oracle"},
+                         "kind": "oracle", "sample": f"float64 numpy oracle; {sample}"},
         "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -661,23 +769,26 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=HEADLINE,
-                    help="headline workload (default: decode B=1, ratio 4); see workloads.make")
-    ap.add_argument("--no-sub", action="store_true", help="headline workload only")
+                    help="headline workload (default: prefill S=8192, ratio 4); see workloads.make")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="the headline workload only (no other configurations or shapes)")
     ap.add_argument("--sub", default=None,
-                    help="comma-separated names: measure only these of the other workloads "
-                         "(attention workloads, kv_write_*, gated_pool_*, indexer_*)")
+                    help="comma-separated names: measure only these of the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-queries", type=int, default=32,
+                    help="reference arm: queries of the call timed per step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.sub is not None:
-        unknown = (set(args.sub.split(",")) - set(SUB_WORKLOADS) - set(KV_WRITES)
-                   - set(GATED_POOLS) - set(INDEXERS))
+        known = (set(sum(CONFIGS.values(), [])) | set(OTHER_SHAPES) | set(KV_WRITES)
+                 | set(GATED_POOLS) | set(INDEXERS) | set(TOPK_SHAPES))
+        unknown = set(args.sub.split(",")) - known
         if unknown:
             ap.error(f"unknown --sub workload(s): {sorted(unknown)}")
     if args.impl == "reference":

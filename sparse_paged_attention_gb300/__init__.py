@@ -23,7 +23,7 @@ __all__ = [
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
     "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
     "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool", "sparse_attn_indexer_logits",
-    "sparse_attn_indexer_topk",
+    "sparse_attn_indexer_topk", "BoundCall", "bind_prefill", "bind_decode",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -265,6 +265,70 @@ def _kv_write(fp8, k, v, positions, pool, *, seq_of_token=None, num_seqs=None, s
             ctypes.byref(c), _stream(stream))
     if st != 0:
         raise SpaError(st, fn.__name__)
+
+
+class BoundCall:
+    """One attention call with its C argument structs built once.
+
+    Calling the object re-issues the same C call on the same tensors (whose contents may change
+    between calls), with no per-call marshalling: what a serving loop or a timing loop wants.  The
+    call goes to the stream given at bind time, or, if none was given, to torch's current stream at
+    the time of the call (so that it can be recorded into a CUDA graph on the capturing stream).
+    The tensors are referenced here, so they stay alive as long as the object does.
+    """
+
+    def __init__(self, fn, args, keep, stream=None):
+        self._fn, self._args, self._keep = fn, args, keep
+        self._stream = None if stream is None else _stream(stream)
+
+    def __call__(self):
+        s = self._stream if self._stream is not None else \
+            torch.cuda.current_stream().cuda_stream
+        st = self._fn(*self._args, s)
+        if st != 0:
+            raise SpaError(st, self._fn.__name__)
+
+
+def bind_prefill(q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_of_token=None,
+                 out=None, num_seqs=None, stream=None, fp8=False) -> BoundCall:
+    """``sparse_attn_paged_prefill[_fp8]`` on fixed tensors, as a zero-argument callable."""
+    lib = load_library()
+    _check_q(q)
+    if out is None:
+        out = torch.empty_like(q)
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    w, c = _pool_c(win, fp8), _pool_c(cmp, fp8)
+    fn = lib.sparse_attn_paged_prefill_fp8 if fp8 else lib.sparse_attn_paged_prefill
+    args = (q.data_ptr(), ctypes.byref(w), ctypes.byref(c) if c is not None else None,
+            ctypes.byref(prob), out.data_ptr())
+    call = BoundCall(fn, args, (q, win, cmp, topk_idx, positions, seq_of_token, out, w, c, prob),
+                     stream)
+    call.out = out
+    return call
+
+
+def bind_decode(q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_of_token=None,
+                out=None, workspace=None, num_seqs=None, stream=None, fp8=False) -> BoundCall:
+    """``sparse_attn_paged_decode[_fp8]`` on fixed tensors, as a zero-argument callable (the
+    workspace, when the plan needs one, is allocated here once)."""
+    lib = load_library()
+    _check_q(q)
+    if out is None:
+        out = torch.empty_like(q)
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    if workspace is None:
+        nbytes = int(lib.sparse_attn_paged_decode_workspace_size(ctypes.byref(prob)))
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    w, c = _pool_c(win, fp8), _pool_c(cmp, fp8)
+    fn = lib.sparse_attn_paged_decode_fp8 if fp8 else lib.sparse_attn_paged_decode
+    args = (q.data_ptr(), ctypes.byref(w), ctypes.byref(c) if c is not None else None,
+            ctypes.byref(prob), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size())
+    call = BoundCall(fn, args, (q, win, cmp, topk_idx, positions, seq_of_token, out, workspace,
+                                w, c, prob), stream)
+    call.out = out
+    call.workspace = workspace
+    return call
 
 
 def sparse_attn_paged_kv_write(k, v, positions, pool, **kw):

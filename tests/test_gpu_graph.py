@@ -68,3 +68,32 @@ def test_graph_replay_equals_eager(name):
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["decode_b1_r4", "prefill_s2048_r4"])
+def test_bound_call_records_on_the_capturing_stream(name):
+    """A call bound once (spa.bind_prefill / bind_decode, no stream given) launches on torch's
+    current stream at call time, so recording it inside a graph capture records the kernel: the
+    replay rewrites out, bit for bit the eager result."""
+    w, dev, q, pos, tk, win, cmp, fn, kw = _setup(name)
+    bind = spa.bind_decode if w.decode else spa.bind_prefill
+    call = bind(q, win, cmp, tk, pos, window=w.window, ratio=w.ratio, scale=w.scale,
+                seq_of_token=kw["seq_of_token"], fp8=w.fp8)
+    call()
+    torch.cuda.synchronize()
+    assert spa.sparse_attn_paged_check_errors() == 0
+    eager = call.out.clone()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        call()
+    call.out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert spa.sparse_attn_paged_check_errors() == 0
+    assert torch.equal(call.out.view(torch.int16), eager.view(torch.int16))

@@ -35,7 +35,8 @@ E4M3_NAN_CODE = 0x7F
 E4M3_MAX = 448.0
 
 __all__ = [
-    "Pool", "Workload", "build", "make", "CONFIG_NAMES", "bf16_bits", "pool_rows_referenced",
+    "Pool", "Workload", "build", "make", "concat_batch", "CONFIG_NAMES", "bf16_bits",
+    "pool_rows_referenced",
 ]
 
 
@@ -311,6 +312,59 @@ def make(name: str, seed: int = 0) -> Workload:
         r = int(r)
         return build(name, seq_positions=[np.arange(0, int(S))], topk=topk_of[r], ratio=r, **big)
     raise KeyError(name)
+
+
+def _stack_tables(tables, offsets):
+    """Block-table rows of several pools stacked, block ids shifted by each pool's offset (-1, an
+    unmapped page, stays -1), padded with -1 to the widest stride."""
+    width = max(int(t.shape[1]) for t in tables)
+    rows = []
+    for t, off in zip(tables, offsets):
+        t = t.to(torch.int64)
+        t = torch.where(t >= 0, t + off, t)
+        pad = torch.full((t.shape[0], width - t.shape[1]), -1, dtype=torch.int64)
+        rows.append(torch.cat([t, pad], dim=1))
+    return torch.cat(rows).to(torch.int32)
+
+
+def _concat_pools(pools):
+    offsets = np.cumsum([0] + [p.num_blocks for p in pools[:-1]]).tolist()
+    kv = torch.cat([p.kv for p in pools])
+    bt = _stack_tables([p.block_table for p in pools], offsets)
+    ks = vs = None
+    if pools[0].k_scale is not None:
+        ks = torch.cat([p.k_scale for p in pools])
+        vs = torch.cat([p.v_scale for p in pools])
+    return Pool(kv, bt, ks, vs)
+
+
+def concat_batch(parts: Sequence[Workload], name: Optional[str] = None) -> Workload:
+    """Independent workloads of one shape as a single batch: their sequences one after the other
+    (sequence ids of part i shifted by the sequences of the parts before it), their pools
+    concatenated (block ids shifted by the blocks before them).  Every query keeps its q, position,
+    top-k list and the row values it reads, so a query's result in the batch is its result in its
+    own part."""
+    w0 = parts[0]
+    for w in parts:
+        for f in ("fp8", "num_heads", "head_dim", "window", "topk", "ratio", "page_size", "scale"):
+            if getattr(w, f) != getattr(w0, f):
+                raise ValueError(f"parts differ in {f}")
+    sot, cmp_entries, base = [], [], 0
+    for w in parts:
+        sot.append(torch.from_numpy(w.seq_ids().astype(np.int32)) + base)
+        cmp_entries += list(w.meta["cmp_entries"])
+        base += w.num_seqs
+    win = _concat_pools([w.win for w in parts])
+    cmp = None if w0.cmp is None else _concat_pools([w.cmp for w in parts])
+    return Workload(name=name or f"{w0.name}_x{len(parts)}", fp8=w0.fp8, decode=w0.decode,
+                    num_heads=w0.num_heads, head_dim=w0.head_dim, window=w0.window,
+                    topk=w0.topk, ratio=w0.ratio, page_size=w0.page_size, scale=w0.scale,
+                    q=torch.cat([w.q for w in parts]),
+                    positions=torch.cat([w.positions for w in parts]),
+                    seq_of_token=torch.cat(sot), topk_idx=torch.cat([w.topk_idx for w in parts]),
+                    win=win, cmp=cmp,
+                    meta={"seed": [w.meta["seed"] for w in parts], "cmp_entries": cmp_entries,
+                          "parts": len(parts)})
 
 
 @dataclass
