@@ -280,6 +280,41 @@ def test_stream_and_repeatability():
     assert torch.equal(d.prefill(), c)
 
 
+@pytest.mark.parametrize("name", ["prefill_s2048_r4", "prefill_s2048_r0", "prefill_fp8_s4096_r4",
+                                  "tiny_r4"])
+def test_back_to_back_calls_are_identical(name):
+    """Many calls queued back to back (no synchronisation between them), eagerly and replayed from
+    a CUDA graph: every output equals the first bit for bit.  The kernels sum each element in one
+    fixed order, so any difference would be a race between the pipeline's roles (a ring slot
+    refilled while still read, a barrier phase taken for the wrong fill)."""
+    d = OnDevice(make(name), _dev())
+    first = d.prefill()
+    torch.cuda.synchronize()
+    check_no_device_error()
+    bind = spa.bind_prefill(d.q, d.win, d.cmp, d.tk, d.pos, fp8=d.w.fp8, **d.kw())
+    outs = []
+    for _ in range(24):
+        bind()
+        outs.append(bind.out.clone())
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        bind()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        for _ in range(4):
+            bind()
+    for _ in range(6):
+        graph.replay()
+        outs.append(bind.out.clone())
+    torch.cuda.synchronize()
+    check_no_device_error()
+    ref = first.view(torch.int16)
+    bad = [i for i, o in enumerate(outs) if not torch.equal(o.view(torch.int16), ref)]
+    assert not bad, f"calls {bad[:8]} differ from the first"
+
+
 # --- e4m3 pools (FreeToken clone PR 3, "Perf/kv fp8 read path") -------------------------------
 
 REL_MEAN_GATE_FP8 = 2e-2
