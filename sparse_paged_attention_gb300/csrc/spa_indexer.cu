@@ -30,14 +30,31 @@ namespace {
 
 constexpr int kTile = kIdxTile;            // key rows per unit (MMA M)
 constexpr int kAAtom = kTile * 128;        // bytes of one 64-dim column of the key tile
-constexpr int kBAtom = kIdxMaxN * 128;     // bytes of one 64-dim column of the query tile
 constexpr int kAOff = 0;
-constexpr int kBOff = 2 * kAAtom;                          // 32 KB
-constexpr int kWOff = kBOff + 2 * kBAtom;                  // 96 KB: weights [8][32] fp32
-constexpr int kPosOff = kWOff + kIdxMaxQ * kIdxHeads * 4;  // positions [8], sequences [8]
-constexpr int kBarOff = kPosOff + 2 * kIdxMaxQ * 4;        // mbarrier (8 B), tmem base, abort
-constexpr int kSmemUsed = kBarOff + 64;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kBOff = 2 * kAAtom;          // 32 KB: the query tile follows the key tile
+constexpr int kIdxCtasPerSm = 4;           // register budget: 128 threads x 128 registers each
+
+// Shared memory and TMEM of a CTA, sized by its group's N = nq * 32 (queries x heads), so that
+// groups of one query (candidate mode, several sequences, decode) leave room for many CTAs per SM
+// where groups of eight fit two:
+//   key tile [2 atoms][128 rows][128 B] | query tile [2 atoms][N rows][128 B] | weights [nq][32]
+//   | positions [8], sequences [8] | mbarrier, TMEM base, abort flag
+struct IdxLayout {
+  int b_atom;          // bytes of one 64-dim column of the query tile (N rows x 128 B)
+  int w_off, pos_off, bar_off, used;
+  uint32_t tmem_cols;  // a power of two >= 32 covering N accumulator columns
+};
+__host__ __device__ inline IdxLayout idx_layout(int nq) {
+  IdxLayout L;
+  const int N = nq * kIdxHeads;
+  L.b_atom = N * 128;                         // multiple of 1024 (N is a multiple of 32)
+  L.w_off = kBOff + 2 * L.b_atom;
+  L.pos_off = L.w_off + nq * kIdxHeads * 4;
+  L.bar_off = L.pos_off + 2 * kIdxMaxQ * 4;
+  L.used = L.bar_off + 64;
+  L.tmem_cols = N <= 32 ? 32u : N <= 64 ? 64u : N <= 128 ? 128u : 256u;
+  return L;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -47,17 +64,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 template <bool kCand>
-__global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerArgs p) {
+__global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm) indexer_kernel(const IndexerArgs p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const IdxLayout L = idx_layout(p.nq);
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5;
-  float* s_w = reinterpret_cast<float*>(sm + kWOff);
-  int* s_pos = reinterpret_cast<int*>(sm + kPosOff);
+  float* s_w = reinterpret_cast<float*>(sm + L.w_off);
+  int* s_pos = reinterpret_cast<int*>(sm + L.pos_off);
   int* s_seq = s_pos + kIdxMaxQ;
-  const uint32_t bar = sb + kBarOff;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kBarOff + 16);
+  const uint32_t bar = sb + L.bar_off;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.bar_off + 16);
 
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -65,11 +83,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerAr
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();  // lane 0 of warp 0 took the branch above; the allocation is warp-collective
-  if (warp == 0) tmem_alloc(sb + kBarOff + 8, kTmemCols);
+  if (warp == 0) tmem_alloc(sb + L.bar_off + 8, L.tmem_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kBarOff + 8);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + L.bar_off + 8);
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
   const int nq = p.nq, N = nq * kIdxHeads;
@@ -94,7 +112,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerAr
         if (ql < nqg)
           v = __ldg(reinterpret_cast<const uint4*>(
               p.q + ((size_t)(q0 + ql) * kIdxHeads + h) * kIdxDim + k * 8));
-        st_shared_v4(sb + kBOff + (k >> 3) * kBAtom + n * 128 + (((k & 7) ^ (n & 7)) << 4), v.x,
+        st_shared_v4(sb + kBOff + (k >> 3) * L.b_atom + n * 128 + (((k & 7) ^ (n & 7)) << 4), v.x,
                      v.y, v.z, v.w);
       }
       for (int idx = tid; idx < nq * kIdxHeads; idx += kIdxThreads) {
@@ -174,7 +192,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerAr
 #pragma unroll
       for (int s = 0; s < 8; ++s) {  // K = 128 in steps of 16: two 64-dim columns of 4 steps
         const uint64_t da = sdesc(sb + kAOff + (s >> 2) * kAAtom + (s & 3) * 32, 16, 1024);
-        const uint64_t db = sdesc(sb + kBOff + (s >> 2) * kBAtom + (s & 3) * 32, 16, 1024);
+        const uint64_t db = sdesc(sb + kBOff + (s >> 2) * L.b_atom + (s & 3) * 32, 16, 1024);
         mma_bf16(tmem, da, db, idesc, s > 0 ? 1u : 0u);
       }
       mma_commit(bar);
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) indexer_kernel(const IndexerAr
   __syncwarp();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, L.tmem_cols);
   }
 }
 
@@ -220,18 +238,27 @@ cudaError_t read_and_clear_indexer_error_word(int* value) {
   return cudaMemcpyToSymbol(g_spa_error, &zero, sizeof(int));
 }
 
-int indexer_smem_bytes() { return kSmemUsed + 1024; }
+int indexer_smem_bytes(int nq) { return idx_layout(nq).used + 1024; }
 
 cudaError_t launch_indexer(const IndexerArgs& a, bool cand, int num_sms, cudaStream_t stream) {
   if (a.nunits == 0) return cudaSuccess;
-  const int smem = indexer_smem_bytes();
-  cudaError_t e = cand ? cudaFuncSetAttribute(indexer_kernel<true>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                       : cudaFuncSetAttribute(indexer_kernel<false>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const IdxLayout L = idx_layout(a.nq);
+  const int smem = indexer_smem_bytes(a.nq);
+  const void* fn = cand ? reinterpret_cast<const void*>(indexer_kernel<true>)
+                        : reinterpret_cast<const void*>(indexer_kernel<false>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       indexer_smem_bytes(kIdxMaxQ));
   if (e != cudaSuccess) return e;
-  // two CTAs per SM (about 100 KB of shared memory and 256 TMEM columns each)
-  const long long grid = a.nunits < 2LL * num_sms ? a.nunits : 2LL * num_sms;
+  // CTAs per SM: what shared memory (228 KB an SM, 1 KB of it reserved per CTA), registers (the
+  // 4 CTAs of the launch bounds) and TMEM (512 columns: a CTA past that would wait in its
+  // allocation for another CTA to end) allow together
+  int per_sm = (228 * 1024) / (smem + 1024);
+  if (per_sm > kIdxCtasPerSm) per_sm = kIdxCtasPerSm;
+  const int tmem_fit = (int)(512u / L.tmem_cols);
+  if (per_sm > tmem_fit) per_sm = tmem_fit;
+  if (per_sm < 1) per_sm = 1;
+  const long long cap = (long long)per_sm * num_sms;
+  const long long grid = a.nunits < cap ? a.nunits : cap;
   if (cand)
     indexer_kernel<true><<<(unsigned)grid, kIdxThreads, smem, stream>>>(a);
   else

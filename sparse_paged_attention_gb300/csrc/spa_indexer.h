@@ -29,7 +29,7 @@ struct IndexerArgs {
   int nq;                       // queries per group (1 .. 8)
   int ntiles;                   // key tiles per query group
 };
-int indexer_smem_bytes();
+int indexer_smem_bytes(int nq);   // dynamic shared memory of a CTA whose groups hold nq queries
 cudaError_t launch_indexer(const IndexerArgs& a, bool cand, int num_sms, cudaStream_t stream);
 cudaError_t read_and_clear_indexer_error_word(int* value);
 
