@@ -2,9 +2,10 @@
 // pools) or quantised to e4m3 with one scale per token and kv_head (FreeToken clone PR 3, "Perf/kv
 // fp8 read path": the per-(token, kv_head) K and V scales its read path folds back in).
 //
-// One warp per (token, K or V) row.  A row of D bf16 values is D / 8 16-byte chunks, at most two
-// per lane (D <= 512): the warp reads the row once, reduces max|x| with shuffles, and writes its
-// codes (8 bytes per chunk) and the scale.  The kernel is bound by HBM: per token it reads 4·D
+// bf16 pools: one warp per (token, K or V) row, copied in 16-byte chunks.  e4m3 pools: one warp per
+// token.  A row of D bf16 values is D / 8 16-byte chunks, at most two per lane (D <= 512): the warp
+// issues the loads of both rows (four chunks a lane) before any arithmetic, reduces each row's
+// max|x| with shuffles, and writes each row's codes (8 bytes per chunk) and scale.  The kernel is bound by HBM: per token it reads 4·D
 // bytes and writes 2·D (e4m3) or 4·D (bf16) bytes plus the scales.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -49,8 +50,8 @@ template <bool kFp8>
 __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteArgs a) {
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp_id >= 2LL * a.T) return;  // (warp-uniform)
-  const int t = (int)(warp_id >> 1), kv = (int)(warp_id & 1);
+  if (warp_id >= (kFp8 ? 1LL : 2LL) * a.T) return;  // (warp-uniform)
+  const int t = kFp8 ? (int)warp_id : (int)(warp_id >> 1), kv = kFp8 ? 0 : (int)(warp_id & 1);
 
   // the slot of the token's position in its sequence's pages
   const int x = __ldg(a.positions + t);
@@ -75,24 +76,41 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const KvWriteArgs a) {
     for (int c = lane; c < nch; c += 32) dst[c] = __ldg(src + c);
     return;
   }
-  uint4 u[2];
-  float amax = 0.f;
+  const uint4* srcv = reinterpret_cast<const uint4*>(a.v + (size_t)t * a.D * 2);
+  uint4 u[2], w[2];
+  float amax = 0.f, vmax = 0.f;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int c = lane + 32 * i;
     u[i] = c < nch ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-    amax = fmaxf(amax, chunk_absmax(u[i]));
+    w[i] = c < nch ? __ldg(srcv + c) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int i = 0; i < 2; ++i) {
+    amax = fmaxf(amax, chunk_absmax(u[i]));
+    vmax = fmaxf(vmax, chunk_absmax(w[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+  }
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-  uint2* dst = reinterpret_cast<uint2*>(a.kv + ((size_t)row * 2 + kv) * a.D);
+  const float vscale = vmax > 0.f ? __fdiv_rn(vmax, 448.f) : 1.f;
+  uint2* dst = reinterpret_cast<uint2*>(a.kv + ((size_t)row * 2) * a.D);
+  uint2* dstv = reinterpret_cast<uint2*>(a.kv + ((size_t)row * 2 + 1) * a.D);
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int c = lane + 32 * i;
-    if (c < nch) dst[c] = chunk_to_e4m3(u[i], scale);
+    if (c < nch) {
+      dst[c] = chunk_to_e4m3(u[i], scale);
+      dstv[c] = chunk_to_e4m3(w[i], vscale);
+    }
   }
-  if (lane == 0) (kv ? a.v_scale : a.k_scale)[row] = scale;
+  if (lane == 0) {
+    a.k_scale[row] = scale;
+    a.v_scale[row] = vscale;
+  }
 }
 
 }  // namespace
@@ -107,7 +125,7 @@ cudaError_t read_and_clear_kv_write_error_word(int* value) {
 
 cudaError_t launch_kv_write(const KvWriteArgs& a, bool fp8, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
-  const long long threads = 2LL * a.T * 32;
+  const long long threads = (fp8 ? 1LL : 2LL) * a.T * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (fp8)
     kv_write_kernel<true><<<blocks, 256, 0, stream>>>(a);
