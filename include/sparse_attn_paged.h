@@ -132,8 +132,8 @@ int sparse_attn_paged_decode_fp8(const void* q, const spa_pool_t* win, const spa
 /*
  * Decode that allocates nothing (the pages have no counterpart: this is a convenience of this
  * library).  For callers that cannot call cudaMalloc where they decode - a host runtime whose
- * device allocator belongs to someone else, or a decode step recorded into a CUDA graph that may
- * not contain allocations.  Same computation and result as sparse_attn_paged_decode, with the
+ * device allocator belongs to someone else, or one with no allocator hooks at that point.  Same
+ * computation and result as sparse_attn_paged_decode, with the
  * caller still passing q, the pools and out.  This entry point always takes the split-K path with
  * global partials and the merge kernel, and its partials go to a scratch array built into the
  * library (SPA_NOALLOC_SCRATCH_BYTES bytes on every device that loads it, held until the process

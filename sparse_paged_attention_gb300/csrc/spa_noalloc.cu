@@ -1,9 +1,9 @@
 // spa_noalloc.cu - decode entry point that allocates nothing.
 //
 // Some callers cannot allocate device memory at the point where they decode: a runtime whose
-// allocator is owned by someone else, an embedded host with no allocator hooks, or a capture of
-// the decode step into a CUDA graph that must not contain allocations.  For them the split-K
-// partials live in a scratch array compiled into this library instead of in a caller workspace.
+// allocator is owned by someone else, or an embedded host with no allocator hooks.  For them the
+// split-K partials live in a scratch array compiled into this library instead of in a caller
+// workspace.
 //
 // The array is a file-scope __device__ object, so every GPU that loads the library holds it
 // until the process exits.  In host code its name is only a host-side stand-in, never a device
