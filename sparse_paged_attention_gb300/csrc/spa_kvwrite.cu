@@ -8,21 +8,18 @@
 // (each contiguous in k and v) into a stage of a four-stage ring.  Eight consumer warps take one
 // token of the group each, read its rows from shared memory, and store them to the token's slot:
 // 16-byte chunks for bf16 pools; for e4m3 pools max|x| by shuffles, then 8 codes per 16-byte chunk
-// (the IEEE fp32 quotients x / scale, rounded to nearest even) and the row's scale.  Each lane
-// resolves the slot of its warp's token 32 groups ahead, so the dependent loads of a slot
+// (the codes of the IEEE fp32 quotients x / scale, spa_kvwrite_quant.cuh) and the row's scale.
+// Each lane resolves the slot of its warp's token 32 groups ahead, so the dependent loads of a slot
 // (position, sequence, block table) overlap the copies.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "spa_kvwrite_quant.cuh"
 #include "spa_launch.h"
 
 namespace spa {
 
 namespace {
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
-  return __uint_as_float(bits16 << 16);
-}
 
 // |x| of the eight bf16 values of a 16-byte chunk, maximum
 __device__ __forceinline__ float chunk_absmax(const uint4& u) {
@@ -30,24 +27,10 @@ __device__ __forceinline__ float chunk_absmax(const uint4& u) {
   float m = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[i] & 0xFFFFu)));
-    m = fmaxf(m, fabsf(bf16_bits_to_f32(w[i] >> 16)));
+    m = fmaxf(m, fabsf(kvq_bf16_to_f32(w[i] & 0xFFFFu)));
+    m = fmaxf(m, fabsf(kvq_bf16_to_f32(w[i] >> 16)));
   }
   return m;
-}
-
-// eight bf16 values / scale (IEEE fp32 division) -> eight e4m3 codes (round to nearest even,
-// saturating), first value in the lowest byte
-__device__ __forceinline__ uint2 chunk_to_e4m3(const uint4& u, float scale) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = __fdiv_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), scale);
-    const float b = __fdiv_rn(bf16_bits_to_f32(w[i] >> 16), scale);
-    c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  }
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 constexpr int kKvwGroup = 8;                          // tokens per stage, one per consumer warp
@@ -197,14 +180,16 @@ __global__ void __launch_bounds__(kKvwThreads, kKvwCtasPerSm) kv_write_kernel(co
         }
         const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
         const float vscale = vmax > 0.f ? __fdiv_rn(vmax, 448.f) : 1.f;
+        const float r = __frcp_rn(scale), vr = __frcp_rn(vscale);
+        const bool fast = kvq_fast_scale(scale), vfast = kvq_fast_scale(vscale);
         uint2* dst = reinterpret_cast<uint2*>(a.kv + (size_t)row * 2 * a.D);
         uint2* dstv = reinterpret_cast<uint2*>(a.kv + ((size_t)row * 2 + 1) * a.D);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int c = lane + 32 * i;
           if (c < nch) {
-            dst[c] = chunk_to_e4m3(u[i], scale);
-            dstv[c] = chunk_to_e4m3(w[i], vscale);
+            dst[c] = kvq_chunk(u[i], scale, r, fast);
+            dstv[c] = kvq_chunk(w[i], vscale, vr, vfast);
           }
         }
         if (lane == 0) {
