@@ -228,6 +228,11 @@ __device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t lbo, uint32
   return d;
 }
 
+// A descriptor moved by `bytes` within shared memory: the start address is bits [0, 14) in 16-byte
+// units, and every address of the CTA's shared memory fits them, so the sum never carries into the
+// next field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // kRes: a resolver warp (the last) walks the page tables of a CTA's next item while the gather
 // warps copy the current one; launched only when CTAs have more than one item.
 // kTma: K/V rows move by tensor-map gathers (CTAs with many items: throughput); otherwise by
@@ -785,19 +790,20 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t dS = tmem + sbuf * M::kSCols;
+          const uint64_t dq0 = sdesc(qbase, 16, 1024);
           for (int kc = 0; kc < n_chunks; ++kc) {
             if (!mbar_wait(BAR(B_FULL + ring), ring_ph, abort_flag)) return false;
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t slot = sb + kRingOff + ring * kSlotBytes;
+            const uint64_t dk0 = sdesc(sb + kRingOff + ring * kSlotBytes, 16, 1024);
             for (int aa = 0; aa < 2; ++aa) {
               const int atom = 2 * kc + aa;
               if (atom >= n_atoms) break;
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
                 if (atom * 4 + ks >= n_ks) break;
-                const uint64_t da = sdesc(slot + aa * kAtomBytes + ks * 32, 16, 1024);
-                const uint64_t db = sdesc(qbase + atom * M::kQAtom + ks * 32, 16, 1024);
+                const uint64_t da = desc_add(dk0, aa * kAtomBytes + ks * 32);
+                const uint64_t db = desc_add(dq0, atom * M::kQAtom + ks * 32);
                 if (kFp8)
                   mma_f8(dS, da, db, idS, (kc | aa | ks) != 0);
                 else
@@ -826,12 +832,13 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
             // A packed tile's slots were waited for by its S just before: issue the MMAs of all
             // head_dim tiles back to back (interleaved, no per-slot wait), then release the slots.
             const int nk = (n + 15) >> 4;
+            const uint64_t dp0 = sdesc(pbase, kAtomBytes, 1024);
+            const uint64_t dv0 = sdesc(sb + kRingOff + v_off, kAtomBytes, 1024);
             for (int kk = 0; kk < nk; ++kk) {
-              const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+              const uint64_t db = desc_add(dp0, kk * 2048);
               int r = ring;
               for (int vc = 0; vc < n_chunks; ++vc) {
-                const uint32_t slot = sb + kRingOff + r * kSlotBytes;
-                const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
+                const uint64_t da = desc_add(dv0, r * kSlotBytes + kk * 2048);
                 mma_bf16(tmem + M::kOCol + vc * 64, da, db, idO, (first && kk == 0) ? 0u : 1u);
                 if (++r == kStages) r = 0;
               }
@@ -852,23 +859,27 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
               // one 128-wide head_dim tile per slot (two 64-wide atoms, LBO apart); K = 16 columns
               const uint32_t dO = tmem + M::kOCol + vc * 64;
               const int nk = (n + 15) >> 4;
+              const uint64_t dv0 = sdesc(slot + v_off, kAtomBytes, 1024);
+              const uint64_t dp0 = sdesc(pbase, kAtomBytes, 1024);
               for (int kk = 0; kk < nk; ++kk) {
-                const uint64_t da = sdesc(slot + v_off + kk * 2048, kAtomBytes, 1024);
-                const uint64_t db = sdesc(pbase + kk * 2048, kAtomBytes, 1024);
+                const uint64_t da = desc_add(dv0, kk * 2048);
+                const uint64_t db = desc_add(dp0, kk * 2048);
                 mma_bf16(dO, da, db, idO, (first && kk == 0) ? 0u : 1u);
               }
             } else {
               // two 128-wide head_dim tiles per slot (one atom each); K = 32 columns; P^T is
               // p_hi (64-byte rows, 64-byte swizzle) followed by p_lo, both into the same O
               const int nk = (n + 31) >> 5;
+              const uint64_t dv0 = sdesc(slot + v_off, kAtomBytes, 1024);
+              const uint64_t dp0 = sdesc64(pbase, 8192, 512);
               for (int aa = 0; aa < 2; ++aa) {
                 const int mt = 2 * vc + aa;
                 if (mt >= n_mt) break;
                 const uint32_t dO = tmem + M::kOCol + mt * 64;
                 for (int kk = 0; kk < nk; ++kk) {
-                  const uint64_t da = sdesc(slot + v_off + aa * kAtomBytes + kk * 4096, kAtomBytes, 1024);
-                  const uint64_t dh = sdesc64(pbase + kk * 2048, 8192, 512);
-                  const uint64_t dl = sdesc64(pbase + 8192 + kk * 2048, 8192, 512);
+                  const uint64_t da = desc_add(dv0, aa * kAtomBytes + kk * 4096);
+                  const uint64_t dh = desc_add(dp0, kk * 2048);
+                  const uint64_t dl = desc_add(dp0, 8192 + kk * 2048);
                   mma_f8(dO, da, dh, idO, (first && kk == 0) ? 0u : 1u);
                   mma_f8(dO, da, dl, idO, 1u);
                 }
