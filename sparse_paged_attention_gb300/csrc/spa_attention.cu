@@ -425,6 +425,8 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
           const int t0 = item / p.n_splits / p.n_groups;
           const int c_lo = s0 * p.cols_per_split;
           const int c_hi = min(C, c_lo + p.cols_per_split);
+          // the first round's top-k entries are read together with the sequence and position
+          const int j0 = c_lo + ptid < c_hi ? column_topk(p.rs, t0, c_lo + ptid) : -1;
           bool seq_ok;
           const int b = seq_of(p.rs, t0, &seq_ok);
           const int pos = __ldg(p.rs.positions + t0);
@@ -432,7 +434,9 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
           float vmax = 0.f;  // largest V scale of the item's columns (e4m3)
           for (int c0 = c_lo; c0 < c_hi; c0 += NGT) {
             const int c = c0 + ptid;
-            const int32_t code = (seq_ok && c < c_hi) ? resolve_column(p.rs, t0, b, pos, c) : -1;
+            const int j = c0 == c_lo ? j0 : (c < c_hi ? column_topk(p.rs, t0, c) : -1);
+            const int32_t code =
+                (seq_ok && c < c_hi) ? column_row(p.rs, b, column_page_j(p.rs, pos, c, j)) : -1;
             if (kFp8 && code >= 0) {
               const float* vs = (code >> kColPoolShift) ? p.rs.cmp.v_scale : p.rs.win.v_scale;
               vmax = fmaxf(vmax, fabsf(__ldg(vs + (code & ((1 << kColPoolShift) - 1)))));

@@ -67,7 +67,15 @@ __device__ __forceinline__ void split_page(int x, const PoolDev& pl, int& page, 
   }
 }
 
-__device__ __forceinline__ ColumnPage column_page(const ResolveArgs& a, int t, int pos, int c) {
+// The top-k entry of column c of query t, or -1 for a window column (or no compressed pool): the
+// one read of a column that does not depend on the query's sequence or position, so a caller can
+// have it in flight together with those.
+__device__ __forceinline__ int column_topk(const ResolveArgs& a, int t, int c) {
+  return (c >= a.W && a.r > 0) ? __ldg(a.topk + (long long)t * a.K + (c - a.W)) : -1;
+}
+
+// column_page given the column's top-k entry j (column_topk).
+__device__ __forceinline__ ColumnPage column_page_j(const ResolveArgs& a, int pos, int c, int j) {
   ColumnPage cp{-1, 0, 0};
   if (c < a.W) {
     const long long x = (long long)pos - a.W + 1 + c;
@@ -85,7 +93,6 @@ __device__ __forceinline__ ColumnPage column_page(const ResolveArgs& a, int t, i
     return cp;
   }
   if (a.r <= 0) return cp;
-  const int j = __ldg(a.topk + (long long)t * a.K + (c - a.W));
   if (j < 0) return cp;
   if ((long long)a.r * j + a.r - 1 > pos) return cp;
   int lp;
@@ -93,6 +100,10 @@ __device__ __forceinline__ ColumnPage column_page(const ResolveArgs& a, int t, i
   cp.pool = 1;
   cp.page = lp < a.cmp.bt_stride ? lp : -1;
   return cp;
+}
+
+__device__ __forceinline__ ColumnPage column_page(const ResolveArgs& a, int t, int pos, int c) {
+  return column_page_j(a, pos, c, column_topk(a, t, c));
 }
 
 __device__ __forceinline__ int32_t column_row(const ResolveArgs& a, int b, const ColumnPage& cp) {
