@@ -5,12 +5,16 @@
 //
 // One CTA per query.  Every scored entry gets a 64-bit key, the logit's order-preserving 32 bits
 // above the complement of its entry index, so that keys are distinct (up to repeated candidates,
-// which are the same entry) and "larger key" is exactly the output order.  An MSB-first radix
-// select (8 bits a pass, 256-bin shared histograms) finds the k-th largest key, stopping as soon
-// as the bucket it lands in holds exactly the entries still needed; one more pass collects the
-// keys above that bucket and the needed ones inside it, and a bitonic sort in shared memory puts
-// the k keys in order.  Each pass re-reads the logits row (from L2 for the sizes the indexer
-// writes); no pass waits on anything but __syncthreads.
+// which are the same entry) and "larger key" is exactly the output order.  The row is read twice:
+//   1. count the scored entries and histogram the keys' top 12 bits (4096 bins in shared memory);
+//      a scan of the bins from the top finds the bucket B holding the take-th largest key;
+//   2. keys above B are selected outright, keys in B are copied to a shared-memory buffer.
+// An MSB-first radix select (8 bits a pass, 256 bins) over the bucket's keys then finds the
+// threshold, stopping as soon as the bucket it lands in holds exactly the keys still needed; the
+// keys above it and the needed ones equal to it are selected.  When B holds more keys than the
+// buffer (many equal logits), the select reads them from the row instead, filtered to B.  A
+// bitonic sort in shared memory puts the k keys in order.  No pass waits on anything but
+// __syncthreads.
 #include "spa_indexer.h"
 #include "spa_indexer_math.cuh"
 
@@ -18,47 +22,159 @@ namespace spa {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kBins = 4096;        // first-pass histogram: the keys' top 12 bits
+constexpr int kBinShift = 52;
+constexpr int kCandMax = 4096;     // keys of bucket B kept in shared memory
+// dynamic shared memory: histogram, selected keys, bucket keys
+constexpr int kSmemBytes = kBins * 4 + kIdxTopkMax * 8 + kCandMax * 8;
 
+// kThreads threads, each loading kUnroll columns before it looks at any of them: 1024 x 16 when
+// there are fewer rows than SMs (a row's two passes are then one SM's latency-bound loop), 512 x 8
+// otherwise (more CTAs per SM).
+template <int kThreads, int kUnroll>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
-  __shared__ unsigned int s_hist[256];
-  __shared__ unsigned long long s_keys[kIdxTopkMax];
-  __shared__ unsigned int s_count, s_eq_taken, s_sel, s_need, s_done;
-  const int tid = threadIdx.x;
+  constexpr int kBinsPerThread = kBins / kThreads;   // bins a thread sums in the bucket scan
+  static_assert(kBins % kThreads == 0 && kBinsPerThread <= 32, "bucket scan");
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned int* s_hist = reinterpret_cast<unsigned int*>(smem);
+  unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(smem + kBins * 4);
+  unsigned long long* s_cand = s_keys + kIdxTopkMax;
+  __shared__ unsigned int s_count, s_ncand, s_eq_taken, s_sel, s_need, s_done;
+  __shared__ unsigned int s_scan[kThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long t = blockIdx.x;
   const float* row = a.logits + t * a.ncols;
   const int32_t* ids = a.cand ? a.cand + t * a.ncols : nullptr;
   const auto entry_of = [&](int c) -> uint32_t { return ids ? (uint32_t)__ldg(ids + c) : (uint32_t)c; };
+  // The keys of columns c0 + u * kThreads + tid, u < kUnroll (0: not scored or past the row; a
+  // scored key is never 0, the order bits of the most negative finite logit being 0x00800000).
+  // All the loads are issued before any key is formed, so a thread has kUnroll of them in flight.
+  const auto row_keys = [&](int c0, unsigned long long (&k)[kUnroll]) {
+    float x[kUnroll];
+    uint32_t id[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int c = c0 + u * kThreads + tid;
+      x[u] = c < a.ncols ? __ldg(row + c) : -INFINITY;
+      id[u] = c < a.ncols ? entry_of(c) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      unsigned long long key;
+      k[u] = topk_order_key(x[u], id[u], key) ? key : 0ull;
+    }
+  };
 
-  // how many entries are scored
+  // ---- pass 1: scored count, histogram of the top 12 bits ----
+  for (int i = tid; i < kBins; i += kThreads) s_hist[i] = 0u;
   if (tid == 0) s_count = 0;
   __syncthreads();
   unsigned int mine = 0;
-  for (int c = tid; c < a.ncols; c += kThreads) {
-    unsigned long long key;
-    mine += topk_order_key(__ldg(row + c), entry_of(c), key) ? 1u : 0u;
+  for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+    unsigned long long k[kUnroll];
+    row_keys(c0, k);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (k[u] == 0ull) continue;
+      ++mine;
+      atomicAdd(&s_hist[k[u] >> kBinShift], 1u);
+    }
   }
   atomicAdd(&s_count, mine);
   __syncthreads();
   const unsigned int scored = s_count;
   const unsigned int take = scored < (unsigned int)a.k ? scored : (unsigned int)a.k;
+  const bool all = take == scored;   // every scored key is selected
 
-  // radix select of the take-th largest key: after the loop, keys whose top (64 - shift) bits
-  // exceed `prefix` are all selected, and `need` of those equal to it
-  unsigned long long prefix = 0ull;
-  int shift = 64;
-  unsigned int need = take;
-  if (take < scored) {
-    for (int pass = 0; pass < 8; ++pass) {
-      const int sh = 56 - 8 * pass;
+  // ---- bucket B of the take-th largest key: thread i holds kBinsPerThread bins, from the top ----
+  if (!all) {
+    unsigned int part = 0;
+#pragma unroll
+    for (int b = 0; b < kBinsPerThread; ++b) part += s_hist[kBins - 1 - kBinsPerThread * tid - b];
+    unsigned int incl = part;   // inclusive scan in thread order (= descending bins)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    __syncthreads();
+    unsigned int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_scan[w];
+    incl += before;
+    const unsigned int excl = incl - part;
+    if (excl < take && incl >= take) {   // exactly one thread: B is among its bins
+      unsigned int cum = excl;
+      for (int b = 0; b < kBinsPerThread; ++b) {
+        const int bin = kBins - 1 - kBinsPerThread * tid - b;
+        const unsigned int h = s_hist[bin];
+        if (cum + h >= take) {
+          s_sel = (unsigned int)bin;
+          s_need = take - cum;
+          break;
+        }
+        cum += h;
+      }
+    }
+  }
+  if (tid == 0) {
+    s_count = 0;
+    s_ncand = 0;
+    s_eq_taken = 0;
+  }
+  __syncthreads();
+  const unsigned long long bucket = all ? 0ull : (unsigned long long)s_sel;
+  unsigned int need = all ? 0u : s_need;
+
+  // ---- pass 2: keys above B are selected, keys in B go to the bucket buffer ----
+  for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+    unsigned long long k[kUnroll];
+    row_keys(c0, k);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const unsigned long long key = k[u];
+      if (key == 0ull) continue;
+      const unsigned long long top = key >> kBinShift;
+      if (all || top > bucket) {
+        s_keys[atomicAdd(&s_count, 1u)] = key;   // fewer than take of them
+      } else if (top == bucket) {
+        const unsigned int slot = atomicAdd(&s_ncand, 1u);
+        if (slot < (unsigned int)kCandMax) s_cand[slot] = key;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (!all) {
+    // the keys of bucket B: from the buffer, or from the row when they did not all fit
+    const unsigned int ncand = s_ncand;
+    const bool in_smem = ncand <= (unsigned int)kCandMax;
+    // f(key) for every key of bucket B
+    const auto for_bucket = [&](auto f) {
+      if (in_smem) {
+        for (int i = tid; i < (int)ncand; i += kThreads) f(s_cand[i]);
+        return;
+      }
+      for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+        unsigned long long k[kUnroll];
+        row_keys(c0, k);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (k[u] != 0ull && (k[u] >> kBinShift) == bucket) f(k[u]);
+      }
+    };
+    // radix select below the top 12 bits: keys whose top (64 - shift) bits exceed `prefix` are
+    // all selected, and `need` of those equal to it
+    unsigned long long prefix = bucket << kBinShift;
+    int shift = kBinShift;
+    while (shift > 0) {
+      const int sh = shift > 8 ? shift - 8 : 0;
+      const unsigned int width_mask = (1u << (shift - sh)) - 1u;
       for (int i = tid; i < 256; i += kThreads) s_hist[i] = 0u;
       __syncthreads();
-      for (int c = tid; c < a.ncols; c += kThreads) {
-        unsigned long long key;
-        if (!topk_order_key(__ldg(row + c), entry_of(c), key)) continue;
-        if (shift < 64 && (key >> shift) != (prefix >> shift)) continue;
-        atomicAdd(&s_hist[(key >> sh) & 0xFFu], 1u);
-      }
+      for_bucket([&](unsigned long long key) {
+        if ((key >> shift) == (prefix >> shift)) atomicAdd(&s_hist[(key >> sh) & width_mask], 1u);
+      });
       __syncthreads();
       if (tid < 32) {  // warp 0: lane l sums bins 255-8l .. 248-8l, scans from the top
         unsigned int part = 0;
@@ -94,30 +210,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       __syncthreads();  // s_sel / s_need / s_done are rewritten by the next pass
       if (done) break;
     }
-  }
-
-  // collect the selected keys (every thread has read s_count: the radix passes may not have run)
-  __syncthreads();
-  if (tid == 0) {
-    s_count = 0;
-    s_eq_taken = 0;
-  }
-  __syncthreads();
-  for (int c = tid; c < a.ncols; c += kThreads) {
-    unsigned long long key;
-    if (!topk_order_key(__ldg(row + c), entry_of(c), key)) continue;
-    bool keep = true;
-    if (shift < 64) {
+    // collect: bucket keys above the threshold, and `need` of those equal to it
+    for_bucket([&](unsigned long long key) {
       const unsigned long long kt = key >> shift, pt = prefix >> shift;
-      if (kt < pt) keep = false;
-      else if (kt == pt) keep = atomicAdd(&s_eq_taken, 1u) < need;
-    }
-    if (keep) {
-      const unsigned int slot = atomicAdd(&s_count, 1u);
-      if (slot < (unsigned int)kIdxTopkMax) s_keys[slot] = key;
-    }
+      bool keep = kt > pt;
+      if (kt == pt) keep = atomicAdd(&s_eq_taken, 1u) < need;
+      if (keep) {
+        const unsigned int slot = atomicAdd(&s_count, 1u);
+        if (slot < (unsigned int)kIdxTopkMax) s_keys[slot] = key;
+      }
+    });
+    __syncthreads();
   }
-  __syncthreads();
 
   // bitonic sort (descending) of the take keys, padded with zeros to a power of two
   int n = 1;
@@ -150,7 +254,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.T == 0 || a.k == 0) return cudaSuccess;
-  topk_kernel<<<(unsigned)a.T, kThreads, 0, stream>>>(a);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const bool few = a.T < sms;
+  const auto kern = few ? topk_kernel<1024, 16> : topk_kernel<512, 8>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)a.T, few ? 1024 : 512, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

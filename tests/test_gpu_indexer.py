@@ -178,7 +178,9 @@ def _topk_logits(T, N, seed, kind):
     return lg
 
 
-@pytest.mark.parametrize("T,N,k", [(4, 300, 16), (3, 65536, 512), (2, 131072, 2048), (5, 700, 900)])
+# 160 rows: more rows than SMs, which the launch gives narrower CTAs (several per SM)
+@pytest.mark.parametrize("T,N,k", [(4, 300, 16), (3, 65536, 512), (2, 131072, 2048), (5, 700, 900),
+                                   (160, 4096, 256)])
 @pytest.mark.parametrize("kind", ["normal", "ties", "sparse"])
 def test_topk_exact(T, N, k, kind):
     dev = _dev()
