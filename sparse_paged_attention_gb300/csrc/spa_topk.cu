@@ -223,13 +223,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     __syncthreads();
   }
 
-  // bitonic sort (descending) of the take keys, padded with zeros to a power of two
+  // bitonic sort (descending) of the take keys, padded with zeros to a power of two.  Stages of
+  // stride 32 and more exchange through shared memory, one barrier each; for every size the stages
+  // of stride below 32 pair elements of one warp (n is a multiple of the warp's 32 elements, or
+  // one warp holds it all) and run together in registers, with shuffles, behind one barrier.
   int n = 1;
   while (n < (int)take) n <<= 1;
   for (int i = (int)take + tid; i < n; i += kThreads) s_keys[i] = 0ull;
   __syncthreads();
   for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    int stride = size >> 1;
+    for (; stride >= 32; stride >>= 1) {
       for (int i = tid; i < n; i += kThreads) {
         const int partner = i ^ stride;
         if (partner > i) {
@@ -243,6 +247,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       }
       __syncthreads();
     }
+    for (int i0 = warp * 32; i0 < n; i0 += kThreads) {   // warp-uniform bounds
+      const int i = i0 + lane;
+      unsigned long long x = i < n ? s_keys[i] : 0ull;
+      const bool desc = (i & size) == 0;
+      for (int st = stride; st > 0; st >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, st);
+        const bool lower = (lane & st) == 0;         // element i is the pair's first
+        x = (lower == desc) ? (x > y ? x : y) : (x < y ? x : y);
+      }
+      if (i < n) s_keys[i] = x;
+    }
+    __syncthreads();
   }
 
   int32_t* out = a.topk + t * a.k;
