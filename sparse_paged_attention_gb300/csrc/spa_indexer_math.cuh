@@ -51,17 +51,27 @@ __host__ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
   return f32_from_bits(s << 23);
 }
 
-// Top-k order key of a scored logit (finite: -inf means "no entry"; +inf and NaN are not
-// scored either): the logit's order-preserving 32 bits (-0 folded into +0) above the complement
-// of the entry index, so that a larger key is a larger logit, or the same logit and a smaller
-// index.
-__host__ __device__ __forceinline__ bool topk_order_key(float x, uint32_t id,
-                                                        unsigned long long& key) {
-  if (!(x > -INFINITY && x < INFINITY)) return false;  // also false for NaN
+// Top-k order bits of a logit: the top 32 bits of its order key, the logit's order-preserving
+// bits (-0 folded into +0), or 0 when the logit is not scored (-inf; +inf and NaN are not scored
+// either).  A scored logit's bits are never 0: the most negative finite logit gives 0x00800000.
+__host__ __device__ __forceinline__ uint32_t topk_order_bits(float x) {
+  if (!(x > -INFINITY && x < INFINITY)) return 0u;  // also 0 for NaN
   if (x == 0.f) x = 0.f;
   const uint32_t u = f32_bits(x);
-  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  key = ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - id);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k order key of a scored logit: its order bits above the complement of the entry index, so
+// that a larger key is a larger logit, or the same logit and a smaller index.
+__host__ __device__ __forceinline__ unsigned long long topk_key(uint32_t order_bits, uint32_t id) {
+  return ((unsigned long long)order_bits << 32) | (unsigned long long)(0xFFFFFFFFu - id);
+}
+
+__host__ __device__ __forceinline__ bool topk_order_key(float x, uint32_t id,
+                                                        unsigned long long& key) {
+  const uint32_t ord = topk_order_bits(x);
+  if (ord == 0u) return false;
+  key = topk_key(ord, id);
   return true;
 }
 

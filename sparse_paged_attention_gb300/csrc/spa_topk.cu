@@ -23,7 +23,8 @@ namespace spa {
 namespace {
 
 constexpr int kBins = 4096;        // first-pass histogram: the keys' top 12 bits
-constexpr int kBinShift = 52;
+constexpr int kBinShift = 52;      // of the 64-bit key
+constexpr int kBinShift32 = 20;    // of its top 32 bits (the order bits)
 constexpr int kCandMax = 4096;     // keys of bucket B kept in shared memory
 // dynamic shared memory: histogram, selected keys, bucket keys
 constexpr int kSmemBytes = kBins * 4 + kIdxTopkMax * 8 + kCandMax * 8;
@@ -46,22 +47,41 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   const float* row = a.logits + t * a.ncols;
   const int32_t* ids = a.cand ? a.cand + t * a.ncols : nullptr;
   const auto entry_of = [&](int c) -> uint32_t { return ids ? (uint32_t)__ldg(ids + c) : (uint32_t)c; };
-  // The keys of columns c0 + u * kThreads + tid, u < kUnroll (0: not scored or past the row; a
-  // scored key is never 0, the order bits of the most negative finite logit being 0x00800000).
-  // All the loads are issued before any key is formed, so a thread has kUnroll of them in flight.
-  const auto row_keys = [&](int c0, unsigned long long (&k)[kUnroll]) {
-    float x[kUnroll];
-    uint32_t id[kUnroll];
+  // A chunk of kThreads * kUnroll columns from c0: the order bits (topk_order_bits: 0 = not scored
+  // or past the row) of a thread's kUnroll columns, all loads issued before any is looked at.  Rows
+  // that start 16-byte aligned with a multiple of 4 columns are read as float4 (thread t takes
+  // columns 4t .. 4t+3 of each kThreads * 4 block), the others one float a thread per kThreads.
+  // The passes need only these bits; the 64-bit key, and a candidate's entry id, are formed for the
+  // few columns that are kept.
+  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0u) && (a.ncols & 3) == 0;
+  const auto col_of = [&](int c0, int u) -> int {
+    return vec ? c0 + 4 * ((u >> 2) * kThreads + tid) + (u & 3) : c0 + u * kThreads + tid;
+  };
+  const auto row_ords = [&](int c0, uint32_t (&o)[kUnroll]) {
+    if (vec) {
+      float4 f[kUnroll / 4];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int c = c0 + u * kThreads + tid;
-      x[u] = c < a.ncols ? __ldg(row + c) : -INFINITY;
-      id[u] = c < a.ncols ? entry_of(c) : 0u;
-    }
+      for (int v = 0; v < kUnroll / 4; ++v) {
+        const int c = c0 + 4 * (v * kThreads + tid);   // the row's length is a multiple of 4
+        f[v] = c < a.ncols ? __ldg(reinterpret_cast<const float4*>(row + c))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      unsigned long long key;
-      k[u] = topk_order_key(x[u], id[u], key) ? key : 0ull;
+      for (int v = 0; v < kUnroll / 4; ++v) {
+        o[4 * v + 0] = topk_order_bits(f[v].x);
+        o[4 * v + 1] = topk_order_bits(f[v].y);
+        o[4 * v + 2] = topk_order_bits(f[v].z);
+        o[4 * v + 3] = topk_order_bits(f[v].w);
+      }
+    } else {
+      float x[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = c0 + u * kThreads + tid;
+        x[u] = c < a.ncols ? __ldg(row + c) : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) o[u] = topk_order_bits(x[u]);
     }
   };
 
@@ -71,13 +91,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   __syncthreads();
   unsigned int mine = 0;
   for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
-    unsigned long long k[kUnroll];
-    row_keys(c0, k);
+    uint32_t o[kUnroll];
+    row_ords(c0, o);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (k[u] == 0ull) continue;
+      if (o[u] == 0u) continue;
       ++mine;
-      atomicAdd(&s_hist[k[u] >> kBinShift], 1u);
+      atomicAdd(&s_hist[o[u] >> kBinShift32], 1u);
     }
   }
   atomicAdd(&s_count, mine);
@@ -123,23 +143,22 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     s_eq_taken = 0;
   }
   __syncthreads();
-  const unsigned long long bucket = all ? 0ull : (unsigned long long)s_sel;
+  const uint32_t bucket = all ? 0u : s_sel;
   unsigned int need = all ? 0u : s_need;
 
   // ---- pass 2: keys above B are selected, keys in B go to the bucket buffer ----
   for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
-    unsigned long long k[kUnroll];
-    row_keys(c0, k);
+    uint32_t o[kUnroll];
+    row_ords(c0, o);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const unsigned long long key = k[u];
-      if (key == 0ull) continue;
-      const unsigned long long top = key >> kBinShift;
+      if (o[u] == 0u) continue;
+      const uint32_t top = o[u] >> kBinShift32;
       if (all || top > bucket) {
-        s_keys[atomicAdd(&s_count, 1u)] = key;   // fewer than take of them
+        s_keys[atomicAdd(&s_count, 1u)] = topk_key(o[u], entry_of(col_of(c0, u)));  // < take
       } else if (top == bucket) {
         const unsigned int slot = atomicAdd(&s_ncand, 1u);
-        if (slot < (unsigned int)kCandMax) s_cand[slot] = key;
+        if (slot < (unsigned int)kCandMax) s_cand[slot] = topk_key(o[u], entry_of(col_of(c0, u)));
       }
     }
   }
@@ -156,16 +175,16 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
         return;
       }
       for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
-        unsigned long long k[kUnroll];
-        row_keys(c0, k);
+        uint32_t o[kUnroll];
+        row_ords(c0, o);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-          if (k[u] != 0ull && (k[u] >> kBinShift) == bucket) f(k[u]);
+          if (o[u] != 0u && (o[u] >> kBinShift32) == bucket) f(topk_key(o[u], entry_of(col_of(c0, u))));
       }
     };
     // radix select below the top 12 bits: keys whose top (64 - shift) bits exceed `prefix` are
     // all selected, and `need` of those equal to it
-    unsigned long long prefix = bucket << kBinShift;
+    unsigned long long prefix = (unsigned long long)bucket << kBinShift;
     int shift = kBinShift;
     while (shift > 0) {
       const int sh = shift > 8 ? shift - 8 : 0;
