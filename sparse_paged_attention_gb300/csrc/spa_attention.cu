@@ -198,15 +198,17 @@ __device__ __forceinline__ float pow2_floor(float x) {
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
-__device__ __forceinline__ float2 e4m3x2_value(uint32_t v) {
-  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&r));
-}
-// (a, b) -> hi = e4m3(a, b), lo = e4m3(a - hi_a, b - hi_b): hi + lo carries about 8 bits.
+// (a, b) -> hi = e4m3(a, b), lo = e4m3(a - hi_a, b - hi_b): hi + lo carries about 8 bits.  The
+// pair is rounded to f16 first (11 bits, far finer than the split's 8; the values are at most 448
+// here) so that the codes, their values and the residual are all packed half arithmetic.
 __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = e4m3x2(a, b);
-  const float2 h = e4m3x2_value(hi);
-  lo = e4m3x2(a - h.x, b - h.y);
+  const __half2 ah = __floats2half2_rn(a, b);
+  hi = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&ah),
+                                            __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)hi, __NV_E4M3);
+  const __half2 res = __hsub2(ah, *reinterpret_cast<const __half2*>(&hr));
+  lo = (uint32_t)__nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&res),
+                                            __NV_SATFINITE, __NV_E4M3);
 }
 
 // Two fp32 values -> packed bf16x2 (round to nearest even), first value in the low half.
