@@ -148,3 +148,19 @@ def test_e4m3_codes_match_ieee_division_for_every_input_pair(tmp_path):
     assert pairs > 10 ** 9
     assert bad == 0, (bad, qdiff)
     assert fast > 0.9 * pairs, (fast, pairs)
+
+
+def test_kv_write_more_than_32_groups_per_cta():
+    """A CTA of the write takes every gridDim-th group of eight tokens, and each lane of a consumer
+    warp resolves its warp's slot 32 groups ahead: with more than 32 groups per CTA (three CTAs
+    per SM) the look-ahead is refilled mid-run.  34 groups per CTA, a partial last group, and a
+    dropped token in a late group: the pool equals the oracle's bit for bit and the drop is
+    flagged."""
+    dev = _dev()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    T = 8 * 3 * sms * 34 + 5
+    inp = kv_write_inputs([np.arange(0, T)], 64, 64, seed=12, specials=False)
+    inp.positions[T - 100] = -1
+    got_kv, got_ks, got_vs, kv_o, ks_o, vs_o, dropped, st = _run(inp, False, dev)
+    assert dropped and st == spa.SPA_STATUS["SPA_ERR_INDEX"]
+    assert np.array_equal(got_kv, kv_o.view(np.uint8).reshape(got_kv.shape))
