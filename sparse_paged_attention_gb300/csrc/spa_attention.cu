@@ -1055,6 +1055,65 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
         arow[lane] = a0;
         arow[32 + lane] = a1;
         __syncwarp();
+        l0 *= a0;
+        l1 *= a1;
+        // pass 2: this column's probabilities and this warp's denominators.  P^T of the column
+        // (bf16: 64 heads x 2 B; e4m3: the hi then the lo codes of 2 x 16 heads per head half) is
+        // parked as 32 words in the TMEM columns of this S buffer that the thread has just read
+        // (half 0 reads columns 0..31 and parks in 0..15, half 1 reads 32..63 and parks in
+        // 16..31; e4m3's lo half of S, 64..127, is read before either).  So the work of pass 2
+        // overlaps PV of the tile before, which still reads the one P buffer in shared memory.
+        // (Parking the first tile of an item too, which has no PV to wait for, measured faster
+        // than storing it straight away.)
+        // (Chunk k of the P^T row: bf16 heads 8k .. 8k+7 at position k ^ (column & 7); e4m3 heads
+        // 16k .. 16k+15 of p_hi, and of p_lo 8 KB on, at position k ^ ((column >> 1) & 3).)
+        uint8_t* const prow = sm + kPOff + tid * (kFp8 ? 64 : 128);
+        const auto store_chunk = [&](int k, const uint32_t* w) {
+          if (!kFp8) {
+            *reinterpret_cast<uint4*>(prow + ((k ^ (tid & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            const int off = (k ^ ((tid >> 1) & 3)) << 4;
+            *reinterpret_cast<uint4*>(prow + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + 8192 + off) = make_uint4(w[8], w[9], w[10], w[11]);
+          }
+        };
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          tmem_ld32(s_addr + hf * 32, x);
+          if (kFp8) {
+            float y[32];
+            tmem_ld32(s_addr + 64 + hf * 32, y);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] += y[k];
+          } else {
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            x[k] = valid ? fast_exp2(x[k] * col_scale - mrow[hf * 32 + k]) : 0.f;
+          uint32_t pw[16];
+          if (!kFp8) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+          } else {
+            // P * v_scale * p_scale as p_hi + p_lo (e4m3): words 0..7 hi, 8..15 lo
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              uint32_t h0, l0v, h1, l1v;
+              split_e4m3x2(x[4 * w + 0] * v_fold, x[4 * w + 1] * v_fold, h0, l0v);
+              split_e4m3x2(x[4 * w + 2] * v_fold, x[4 * w + 3] * v_fold, h1, l1v);
+              pw[w] = h0 | (h1 << 16);
+              pw[8 + w] = l0v | (l1v << 16);
+            }
+          }
+          tmem_st16(s_addr + hf * 16, pw);
+          const float ts = xreduce32<false>(x, lane);
+          if (hf == 0) l0 += ts; else l1 += ts;
+        }
+        tmem_wait_st();
         if (!first) {
           // wait for PV of the tile before (the MMA warp issues S of a tile before PV of the
           // one before it): then O can be rescaled and the P buffer reused
@@ -1078,64 +1137,21 @@ __global__ void __launch_bounds__(attn_threads(kTma, kRes), 1)
           }
           tmem_wait_st();
         }
-        l0 *= a0;
-        l1 *= a1;
-        // pass 2: probabilities, P^T row of this column, this warp's denominators
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[32];
-          tmem_ld32(s_addr + hf * 32, x);
-          if (kFp8) {
-            float y[32];
-            tmem_ld32(s_addr + 64 + hf * 32, y);
-            tmem_wait_ld();
+        {
+          // the parked P^T row into the P buffer
+          float pf[32];
+          tmem_ld32(s_addr, pf);
+          tmem_wait_ld();
+          uint32_t pw[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] += y[k];
-          } else {
-            tmem_wait_ld();
-          }
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            x[k] = valid ? fast_exp2(x[k] * col_scale - mrow[hf * 32 + k]) : 0.f;
+          for (int k = 0; k < 32; ++k) pw[k] = __float_as_uint(pf[k]);
           if (!kFp8) {
-            uint8_t* prow = sm + kPOff + tid * 128;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int k = hf * 4 + q4;  // 16-byte chunk: heads 8k .. 8k+7
-              uint4 u;
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(x[8 * q4 + 0], x[8 * q4 + 1]);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(x[8 * q4 + 2], x[8 * q4 + 3]);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q4 + 4], x[8 * q4 + 5]);
-              __nv_bfloat162 b3 = __floats2bfloat162_rn(x[8 * q4 + 6], x[8 * q4 + 7]);
-              u.x = *reinterpret_cast<uint32_t*>(&b0);
-              u.y = *reinterpret_cast<uint32_t*>(&b1);
-              u.z = *reinterpret_cast<uint32_t*>(&b2);
-              u.w = *reinterpret_cast<uint32_t*>(&b3);
-              *reinterpret_cast<uint4*>(prow + ((k ^ (tid & 7)) << 4)) = u;
-            }
+            for (int k = 0; k < 8; ++k) store_chunk(k, pw + 4 * k);
           } else {
-            // P * v_scale * p_scale as p_hi + p_lo (e4m3), 64-byte rows, 64-byte swizzle
-            uint8_t* ph = sm + kPOff + tid * 64;
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              const int k = hf * 2 + q2;  // 16-byte chunk: heads 16k .. 16k+15
-              uint32_t hi[4], lo[4];
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                uint32_t h0, l0v, h1, l1v;
-                const float* xv = x + 16 * q2 + 4 * w;
-                split_e4m3x2(xv[0] * v_fold, xv[1] * v_fold, h0, l0v);
-                split_e4m3x2(xv[2] * v_fold, xv[3] * v_fold, h1, l1v);
-                hi[w] = h0 | (h1 << 16);
-                lo[w] = l0v | (l1v << 16);
-              }
-              const int off = (k ^ ((tid >> 1) & 3)) << 4;
-              *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4*>(ph + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
+            for (int k = 0; k < 4; ++k) store_chunk(k, pw + (k >> 1) * 16 + (k & 1) * 4);
           }
-          const float ts = xreduce32<false>(x, lane);
-          if (hf == 0) l0 += ts; else l1 += ts;
         }
         tc_fence_before();
         mbar_arrive(BAR(B_SEMPTY + sbuf));
