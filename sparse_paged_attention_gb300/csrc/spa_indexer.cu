@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm) indexer_kernel(con
       float scale[4];
 #pragma unroll
       for (int s = 0; s < 4; ++s) scale[s] = e8m0_to_f32((words[16] >> (8 * s)) & 0xFFu);
+      // a NaN scale (byte 0xFF) keeps the per-code path, whose NaN carries the code's sign
 #pragma unroll
       for (int w = 0; w < 16; ++w) {  // word w: dims 8w .. 8w+7, one 16-byte chunk of the row
         const float sc = scale[w >> 2];
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm) indexer_kernel(con
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t byte = (words[w] >> (8 * e)) & 0xFFu;
-          pk[e] = e2m1_to_bf16_bits(byte & 0xFu, sc) | (e2m1_to_bf16_bits(byte >> 4, sc) << 16);
+          pk[e] = e2m1x2_to_bf16x2_bits(byte, sc);
         }
         st_shared_v4(sb + kAOff + (w >> 3) * kAAtom + tid * 128 + (((w & 7) ^ (tid & 7)) << 4),
                      pk[0], pk[1], pk[2], pk[3]);

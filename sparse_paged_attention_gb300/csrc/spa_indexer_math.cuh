@@ -2,7 +2,8 @@
 // so that the very code the kernels run can be checked on a CPU against the oracle.
 //
 //   e2m1_to_bf16_bits / e8m0_to_f32: the fp4_e8m0_b32 key-row decoding (OCP MX E2M1 codes, E8M0
-//   scales), every product exact in bf16 (FreeToken PR 634, "Correctness and tests").
+//   scales), every product exact in bf16 (FreeToken PR 634, "Correctness and tests");
+//   e2m1x2_to_bf16x2_bits: the same for a pair of codes, on the device.
 //   topk_order_key: the 64-bit key whose order is the top-k output order.
 #pragma once
 
@@ -10,6 +11,8 @@
 #include <cstring>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
 
 namespace spa {
 
@@ -43,6 +46,23 @@ __host__ __device__ __forceinline__ uint32_t e2m1_to_bf16_bits(uint32_t c, float
   const float v = f32_from_bits(mag) * scale;
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) | ((c & 8u) << 12);
 }
+
+#ifdef __CUDACC__
+// Two e2m1 codes (the byte's low nibble first) times a scale -> bf16x2 bits, the first code's
+// value in the low half: the same bits as e2m1_to_bf16_bits for each code (the code's value is
+// exact in f16 and in fp32, its product with the scale is the same fp32 product, rounded to bf16
+// the same way; the sign is the code's, carried through the product), for every scale but the NaN
+// one, where both give a NaN and only its sign bit may differ.  The pair conversion is one
+// instruction where e2m1_to_bf16_bits builds each magnitude, and the kernel's unrolled decoding
+// loop stays small (it is instruction-cache bound: keeping the per-code path beside this one, for
+// NaN scales, cost a fifth of the full-prefill speed).
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2_bits(uint32_t byte, float scale) {
+  const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)byte, __NV_E2M1);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+#endif
 
 // ue8m0 scale byte -> fp32: 2^(s - 127); 0 is the fp32 subnormal 2^-127; 0xFF is NaN.
 __host__ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {

@@ -198,3 +198,26 @@ def test_topk_candidate_ids():
     got = spa.sparse_attn_indexer_topk(torch.from_numpy(lg).to(dev), 512,
                                        cand=torch.from_numpy(cand).to(dev)).cpu().numpy()
     assert np.array_equal(got, oi.topk_entries(lg.astype(np.float64), 512, cand=cand))
+
+
+def test_paired_key_decoding_equals_per_code_decoding(tmp_path):
+    """The indexer decodes key bytes two codes at a time (e2m1x2_to_bf16x2_bits in
+    sparse_paged_attention_gb300/csrc/spa_indexer_math.cuh): for every byte and every ue8m0 scale
+    but the NaN one, the bits equal the per-code decoding that the host test checks against the
+    oracle (tests/indexer_dequant_check.cu)."""
+    import os
+    import shutil
+    import subprocess
+    _dev()
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    exe = str(tmp_path / "indexer_dequant_check")
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                        "-I", os.path.join(root, "sparse_paged_attention_gb300", "csrc"),
+                        os.path.join(root, "tests", "indexer_dequant_check.cu"), "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    pairs, bad = (int(v) for v in out.stdout.split())
+    assert pairs == 255 * 256 and bad == 0, (pairs, bad)
