@@ -3,7 +3,7 @@
 // entry index, -1 filling the list when fewer than k were scored.  The result is the attention's
 // top-k list.
 //
-// One CTA per query.  Every scored entry gets a 64-bit key, the logit's order-preserving 32 bits
+// One CTA (or one cluster of CTAs) per query.  Every scored entry gets a 64-bit key, the logit's order-preserving 32 bits
 // above the complement of its entry index, so that keys are distinct (up to repeated candidates,
 // which are the same entry) and "larger key" is exactly the output order.  The row is read twice:
 //   1. count the scored entries and histogram the keys' top 12 bits (4096 bins in shared memory);
@@ -14,7 +14,8 @@
 // keys above it and the needed ones equal to it are selected.  When B holds more keys than the
 // buffer (many equal logits), the select reads them from the row instead, filtered to B.  A
 // bitonic sort in shared memory puts the k keys in order.  No pass waits on anything but
-// __syncthreads.
+// __syncthreads, and, when a cluster of CTAs shares a row (few rows), three cluster barriers that
+// every thread passes.
 #include "spa_indexer.h"
 #include "spa_indexer_math.cuh"
 
@@ -29,10 +30,38 @@ constexpr int kCandMax = 4096;     // keys of bucket B kept in shared memory
 // dynamic shared memory: histogram, selected keys, bucket keys
 constexpr int kSmemBytes = kBins * 4 + kIdxTopkMax * 8 + kCandMax * 8;
 
+// Distributed shared memory between the CTAs of a cluster (one row per cluster).
+__device__ __forceinline__ unsigned int ld_cluster_u32(uint32_t addr) {
+  unsigned int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_add_cluster(uint32_t addr, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+// Every thread of every CTA of the cluster; shared-memory writes before it are seen after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  cluster_arrive();
+  cluster_wait();
+}
+
 // kThreads threads, each loading kUnroll columns before it looks at any of them: 1024 x 16 when
 // there are fewer rows than SMs (a row's two passes are then one SM's latency-bound loop), 512 x 8
-// otherwise (more CTAs per SM).
-template <int kThreads, int kUnroll>
+// otherwise (more CTAs per SM).  kCluster > 1: a cluster of kCluster CTAs per row (for a few rows),
+// each taking one chunk of the row through both passes:
+//   - after pass 1 (cluster barrier 1) CTA r sums bins [r, r + 1) * kBins / kCluster of every
+//     CTA's histogram, and the row's scored count;
+//   - after cluster barrier 2 every CTA copies the summed histogram and finds the same bucket B;
+//   - pass 2 appends each CTA's kept keys and bucket keys to CTA 0's buffers (remote atomics);
+//   - after cluster barrier 3 CTA 0 selects and sorts as a single CTA would.
+// Every thread of every CTA passes the three barriers, whatever the row holds.
+template <int kThreads, int kUnroll, int kCluster>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   constexpr int kBinsPerThread = kBins / kThreads;   // bins a thread sums in the bucket scan
   static_assert(kBins % kThreads == 0 && kBinsPerThread <= 32, "bucket scan");
@@ -40,10 +69,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   unsigned int* s_hist = reinterpret_cast<unsigned int*>(smem);
   unsigned long long* s_keys = reinterpret_cast<unsigned long long*>(smem + kBins * 4);
   unsigned long long* s_cand = s_keys + kIdxTopkMax;
-  __shared__ unsigned int s_count, s_ncand, s_eq_taken, s_sel, s_need, s_done;
+  __shared__ unsigned int s_count, s_kcnt, s_ncand, s_eq_taken, s_sel, s_need, s_done, s_total;
   __shared__ unsigned int s_scan[kThreads / 32];
+  __shared__ unsigned int s_red[kCluster > 1 ? kBins / kCluster : 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long t = blockIdx.x;
+  const long long t = blockIdx.x / kCluster;
+  const int rank = kCluster > 1 ? (int)cluster_ctarank() : 0;
+  // this CTA's columns: the whole row, or its chunk (a multiple of 4 columns: float4 alignment)
+  const int chunk = kCluster > 1 ? (((a.ncols + kCluster - 1) / kCluster + 3) & ~3) : a.ncols;
+  const int cbeg = min(a.ncols, rank * chunk), cend = min(a.ncols, cbeg + chunk);
   const float* row = a.logits + t * a.ncols;
   const int32_t* ids = a.cand ? a.cand + t * a.ncols : nullptr;
   const auto entry_of = [&](int c) -> uint32_t { return ids ? (uint32_t)__ldg(ids + c) : (uint32_t)c; };
@@ -57,14 +91,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   const auto col_of = [&](int c0, int u) -> int {
     return vec ? c0 + 4 * ((u >> 2) * kThreads + tid) + (u & 3) : c0 + u * kThreads + tid;
   };
-  const auto row_ords = [&](int c0, uint32_t (&o)[kUnroll]) {
+  const auto row_ords = [&](int c0, uint32_t (&o)[kUnroll], int cend_) {
     if (vec) {
       float4 f[kUnroll / 4];
 #pragma unroll
       for (int v = 0; v < kUnroll / 4; ++v) {
         const int c = c0 + 4 * (v * kThreads + tid);   // the row's length is a multiple of 4
-        f[v] = c < a.ncols ? __ldg(reinterpret_cast<const float4*>(row + c))
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        f[v] = c < cend_ ? __ldg(reinterpret_cast<const float4*>(row + c))
+                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
       for (int v = 0; v < kUnroll / 4; ++v) {
@@ -78,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * kThreads + tid;
-        x[u] = c < a.ncols ? __ldg(row + c) : -INFINITY;
+        x[u] = c < cend_ ? __ldg(row + c) : -INFINITY;
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) o[u] = topk_order_bits(x[u]);
@@ -87,12 +121,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 
   // ---- pass 1: scored count, histogram of the top 12 bits ----
   for (int i = tid; i < kBins; i += kThreads) s_hist[i] = 0u;
-  if (tid == 0) s_count = 0;
+  if (tid == 0) {
+    s_count = 0;
+    s_kcnt = 0;
+    s_ncand = 0;
+    s_eq_taken = 0;
+  }
   __syncthreads();
   unsigned int mine = 0;
-  for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+  for (int c0 = cbeg; c0 < cend; c0 += kThreads * kUnroll) {
     uint32_t o[kUnroll];
-    row_ords(c0, o);
+    row_ords(c0, o, cend);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (o[u] == 0u) continue;
@@ -102,7 +141,28 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   }
   atomicAdd(&s_count, mine);
   __syncthreads();
-  const unsigned int scored = s_count;
+  if constexpr (kCluster > 1) {
+    constexpr int kSlice = kBins / kCluster;
+    cluster_sync_all();   // 1: every CTA's histogram and count are complete
+    for (int i = tid; i < kSlice; i += kThreads) {
+      const uint32_t bin = smem_u32(&s_hist[rank * kSlice + i]);
+      unsigned int sum = 0;
+#pragma unroll
+      for (int k = 0; k < kCluster; ++k) sum += ld_cluster_u32(mapa_cluster(bin, (uint32_t)k));
+      s_red[i] = sum;
+    }
+    if (tid == 0) {
+      unsigned int tot = 0;
+#pragma unroll
+      for (int k = 0; k < kCluster; ++k) tot += ld_cluster_u32(mapa_cluster(smem_u32(&s_count), (uint32_t)k));
+      s_total = tot;
+    }
+    cluster_sync_all();   // 2: every slice is summed; no CTA reads another's histogram any more
+    for (int i = tid; i < kBins; i += kThreads)
+      s_hist[i] = ld_cluster_u32(mapa_cluster(smem_u32(&s_red[i % kSlice]), (uint32_t)(i / kSlice)));
+    __syncthreads();
+  }
+  const unsigned int scored = kCluster > 1 ? s_total : s_count;
   const unsigned int take = scored < (unsigned int)a.k ? scored : (unsigned int)a.k;
   const bool all = take == scored;   // every scored key is selected
 
@@ -137,32 +197,45 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       }
     }
   }
-  if (tid == 0) {
-    s_count = 0;
-    s_ncand = 0;
-    s_eq_taken = 0;
-  }
   __syncthreads();
   const uint32_t bucket = all ? 0u : s_sel;
   unsigned int need = all ? 0u : s_need;
 
   // ---- pass 2: keys above B are selected, keys in B go to the bucket buffer ----
-  for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+  // (a cluster: to CTA 0's buffers)
+  const auto keep_key = [&](unsigned long long key) {   // fewer than take of them
+    if constexpr (kCluster > 1) {
+      const unsigned int slot = atom_add_cluster(mapa_cluster(smem_u32(&s_kcnt), 0u), 1u);
+      st_cluster_u64(mapa_cluster(smem_u32(&s_keys[slot]), 0u), key);
+    } else {
+      s_keys[atomicAdd(&s_kcnt, 1u)] = key;
+    }
+  };
+  const auto bucket_keep = [&](unsigned long long key) {
+    if constexpr (kCluster > 1) {
+      const unsigned int slot = atom_add_cluster(mapa_cluster(smem_u32(&s_ncand), 0u), 1u);
+      if (slot < (unsigned int)kCandMax) st_cluster_u64(mapa_cluster(smem_u32(&s_cand[slot]), 0u), key);
+    } else {
+      const unsigned int slot = atomicAdd(&s_ncand, 1u);
+      if (slot < (unsigned int)kCandMax) s_cand[slot] = key;
+    }
+  };
+  for (int c0 = cbeg; c0 < cend; c0 += kThreads * kUnroll) {
     uint32_t o[kUnroll];
-    row_ords(c0, o);
+    row_ords(c0, o, cend);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (o[u] == 0u) continue;
       const uint32_t top = o[u] >> kBinShift32;
-      if (all || top > bucket) {
-        s_keys[atomicAdd(&s_count, 1u)] = topk_key(o[u], entry_of(col_of(c0, u)));  // < take
-      } else if (top == bucket) {
-        const unsigned int slot = atomicAdd(&s_ncand, 1u);
-        if (slot < (unsigned int)kCandMax) s_cand[slot] = topk_key(o[u], entry_of(col_of(c0, u)));
-      }
+      if (all || top > bucket) keep_key(topk_key(o[u], entry_of(col_of(c0, u))));
+      else if (top == bucket) bucket_keep(topk_key(o[u], entry_of(col_of(c0, u))));
     }
   }
   __syncthreads();
+  if constexpr (kCluster > 1) {
+    cluster_sync_all();   // 3: every CTA's keys are in CTA 0; the other CTAs are done
+    if (rank != 0) return;
+  }
 
   if (!all) {
     // the keys of bucket B: from the buffer, or from the row when they did not all fit
@@ -174,9 +247,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
         for (int i = tid; i < (int)ncand; i += kThreads) f(s_cand[i]);
         return;
       }
-      for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {
+      for (int c0 = 0; c0 < a.ncols; c0 += kThreads * kUnroll) {   // the whole row
         uint32_t o[kUnroll];
-        row_ords(c0, o);
+        row_ords(c0, o, a.ncols);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
           if (o[u] != 0u && (o[u] >> kBinShift32) == bucket) f(topk_key(o[u], entry_of(col_of(c0, u))));
@@ -235,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
       bool keep = kt > pt;
       if (kt == pt) keep = atomicAdd(&s_eq_taken, 1u) < need;
       if (keep) {
-        const unsigned int slot = atomicAdd(&s_count, 1u);
+        const unsigned int slot = atomicAdd(&s_kcnt, 1u);
         if (slot < (unsigned int)kIdxTopkMax) s_keys[slot] = key;
       }
     });
@@ -285,6 +358,31 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     out[i] = i < (int)take ? (int32_t)(0xFFFFFFFFu - (uint32_t)(s_keys[i] & 0xFFFFFFFFull)) : -1;
 }
 
+// One row per cluster of kCluster CTAs.
+template <int kThreads, int kUnroll, int kCluster>
+cudaError_t launch_topk_cluster(const TopkArgs& a, cudaStream_t stream, bool query_only,
+                                int* max_clusters) {
+  const auto kern = topk_kernel<kThreads, kUnroll, kCluster>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && kCluster > 8)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t c = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCluster;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  c.gridDim = dim3((unsigned)(a.T * kCluster));
+  c.blockDim = dim3(kThreads);
+  c.dynamicSmemBytes = kSmemBytes;
+  c.stream = stream;
+  c.attrs = at;
+  c.numAttrs = 1;
+  if (query_only) return cudaOccupancyMaxActiveClusters(max_clusters, kern, &c);
+  return cudaLaunchKernelEx(&c, kern, a);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -293,8 +391,22 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  // A few rows: a cluster of CTAs per row, 16 (a non-portable size, if this device can place one)
+  // or 8.  16 CTAs of 4096 columns take one row of 65,536 in 18.4 us, 8 of 8192 in 20.5 us, one
+  // CTA in 30.7 us (GB300, L2 flushed).
+  static int c16_fits[64];   // per device: 0 unknown, 1 yes, 2 no
+  if ((long long)a.T * 16 <= sms && dev < 64) {
+    if (c16_fits[dev] == 0) {
+      int n = 0;
+      e = launch_topk_cluster<512, 8, 16>(a, stream, true, &n);
+      if (e != cudaSuccess) (void)cudaGetLastError();
+      c16_fits[dev] = (e == cudaSuccess && n >= 1) ? 1 : 2;
+    }
+    if (c16_fits[dev] == 1) return launch_topk_cluster<512, 8, 16>(a, stream, false, nullptr);
+  }
+  if ((long long)a.T * 8 <= sms) return launch_topk_cluster<512, 16, 8>(a, stream, false, nullptr);
   const bool few = a.T < sms;
-  const auto kern = few ? topk_kernel<1024, 16> : topk_kernel<512, 8>;
+  const auto kern = few ? topk_kernel<1024, 16, 1> : topk_kernel<512, 8, 1>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)a.T, few ? 1024 : 512, kSmemBytes, stream>>>(a);

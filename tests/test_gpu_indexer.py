@@ -178,9 +178,13 @@ def _topk_logits(T, N, seed, kind):
     return lg
 
 
-# 160 rows: more rows than SMs, which the launch gives narrower CTAs (several per SM)
+# Up to a sixteenth as many rows as SMs take a cluster of 16 CTAs per row, up to an eighth a
+# cluster of 8 (12 rows), the row split in chunks (1001 and 4099 columns are not multiples of 4;
+# 7 columns leave most CTAs of the cluster without any); 40 rows take one wide CTA per row; 160
+# rows, more than SMs, take narrower CTAs (several per SM).
 @pytest.mark.parametrize("T,N,k", [(4, 300, 16), (3, 65536, 512), (2, 131072, 2048), (5, 700, 900),
-                                   (160, 4096, 256)])
+                                   (3, 1001, 64), (2, 7, 4), (12, 4099, 700), (12, 65536, 2048),
+                                   (40, 2051, 300), (160, 4096, 256)])
 @pytest.mark.parametrize("kind", ["normal", "ties", "sparse"])
 def test_topk_exact(T, N, k, kind):
     dev = _dev()
