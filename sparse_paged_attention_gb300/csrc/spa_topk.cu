@@ -3,9 +3,10 @@
 // entry index, -1 filling the list when fewer than k were scored.  The result is the attention's
 // top-k list.
 //
-// One CTA (or one cluster of CTAs) per query.  Every scored entry gets a 64-bit key, the logit's order-preserving 32 bits
-// above the complement of its entry index, so that keys are distinct (up to repeated candidates,
-// which are the same entry) and "larger key" is exactly the output order.  The row is read twice:
+// One CTA (or one cluster of CTAs) per query.  Every scored entry gets a 64-bit key, the logit's
+// order-preserving 32 bits above the complement of its entry index, so that keys are distinct (up
+// to repeated candidates, which are the same entry) and "larger key" is exactly the output order.
+// The row is read twice:
 //   1. count the scored entries and histogram the keys' top 12 bits (4096 bins in shared memory);
 //      a scan of the bins from the top finds the bucket B holding the take-th largest key;
 //   2. keys above B are selected outright, keys in B are copied to a shared-memory buffer.
