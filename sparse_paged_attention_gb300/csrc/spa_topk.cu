@@ -14,9 +14,9 @@
 // threshold, stopping as soon as the bucket it lands in holds exactly the keys still needed; the
 // keys above it and the needed ones equal to it are selected.  When B holds more keys than the
 // buffer (many equal logits), the select reads them from the row instead, filtered to B.  A
-// bitonic sort in shared memory puts the k keys in order.  No pass waits on anything but
-// __syncthreads, and, when a cluster of CTAs shares a row (few rows), three cluster barriers that
-// every thread passes.
+// bitonic sort in shared memory puts the k keys in order (a cluster of CTAs that shares a row
+// ranks them instead, below).  No pass waits on anything but __syncthreads and, in a cluster,
+// cluster barriers that every thread passes.
 #include "spa_indexer.h"
 #include "spa_indexer_math.cuh"
 
@@ -35,6 +35,11 @@ constexpr int kSmemBytes = kBins * 4 + kIdxTopkMax * 8 + kCandMax * 8;
 __device__ __forceinline__ unsigned int ld_cluster_u32(uint32_t addr) {
   unsigned int v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
@@ -60,10 +65,16 @@ __device__ __forceinline__ void cluster_sync_all() {
 //     CTA's histogram, and the row's scored count;
 //   - after cluster barrier 2 every CTA copies the summed histogram and finds the same bucket B;
 //   - pass 2 appends each CTA's kept keys and bucket keys to CTA 0's buffers (remote atomics);
-//   - after cluster barrier 3 CTA 0 selects and sorts as a single CTA would.
-// Every thread of every CTA passes the three barriers, whatever the row holds.
+//   - after cluster barrier 3 CTA 0 selects as a single CTA would;
+//   - after cluster barrier 4 every CTA copies the selected keys and writes the output positions
+//     of its share of them (a key's rank: the number of keys above it), in place of a sort;
+//   - a last split barrier keeps CTA 0 resident until every copy from it is done.
+// Every thread of every CTA passes every barrier, whatever the row holds.
+// (three 512-thread CTAs an SM for many rows, whose 64 KB of shared memory allows three; two for
+// a cluster's CTAs, so that the clusters of up to 19 rows are all resident together)
 template <int kThreads, int kUnroll, int kCluster>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 ? 3 : 1))
+    topk_kernel(const TopkArgs a) {
   constexpr int kBinsPerThread = kBins / kThreads;   // bins a thread sums in the bucket scan
   static_assert(kBins % kThreads == 0 && kBinsPerThread <= 32, "bucket scan");
   extern __shared__ __align__(16) unsigned char smem[];
@@ -147,20 +158,35 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     cluster_sync_all();   // 1: every CTA's histogram and count are complete
     for (int i = tid; i < kSlice; i += kThreads) {
       const uint32_t bin = smem_u32(&s_hist[rank * kSlice + i]);
+      unsigned int v[kCluster];   // all loads in flight before the sum
+#pragma unroll
+      for (int k = 0; k < kCluster; ++k) v[k] = ld_cluster_u32(mapa_cluster(bin, (uint32_t)k));
       unsigned int sum = 0;
 #pragma unroll
-      for (int k = 0; k < kCluster; ++k) sum += ld_cluster_u32(mapa_cluster(bin, (uint32_t)k));
+      for (int k = 0; k < kCluster; ++k) sum += v[k];
       s_red[i] = sum;
     }
     if (tid == 0) {
+      unsigned int v[kCluster];
+#pragma unroll
+      for (int k = 0; k < kCluster; ++k) v[k] = ld_cluster_u32(mapa_cluster(smem_u32(&s_count), (uint32_t)k));
       unsigned int tot = 0;
 #pragma unroll
-      for (int k = 0; k < kCluster; ++k) tot += ld_cluster_u32(mapa_cluster(smem_u32(&s_count), (uint32_t)k));
+      for (int k = 0; k < kCluster; ++k) tot += v[k];
       s_total = tot;
     }
     cluster_sync_all();   // 2: every slice is summed; no CTA reads another's histogram any more
-    for (int i = tid; i < kBins; i += kThreads)
-      s_hist[i] = ld_cluster_u32(mapa_cluster(smem_u32(&s_red[i % kSlice]), (uint32_t)(i / kSlice)));
+    {
+      constexpr int kPer = kBins / kThreads;
+      unsigned int v[kPer];   // all loads in flight before the stores
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int i = tid + m * kThreads;
+        v[m] = ld_cluster_u32(mapa_cluster(smem_u32(&s_red[i % kSlice]), (uint32_t)(i / kSlice)));
+      }
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) s_hist[tid + m * kThreads] = v[m];
+    }
     __syncthreads();
   }
   const unsigned int scored = kCluster > 1 ? s_total : s_count;
@@ -233,12 +259,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     }
   }
   __syncthreads();
-  if constexpr (kCluster > 1) {
-    cluster_sync_all();   // 3: every CTA's keys are in CTA 0; the other CTAs are done
-    if (rank != 0) return;
-  }
+  if constexpr (kCluster > 1) cluster_sync_all();   // 3: every CTA's keys are in CTA 0
 
-  if (!all) {
+  if (!all && rank == 0) {
     // the keys of bucket B: from the buffer, or from the row when they did not all fit
     const unsigned int ncand = s_ncand;
     const bool in_smem = ncand <= (unsigned int)kCandMax;
@@ -316,6 +339,50 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     __syncthreads();
   }
 
+  int32_t* out = a.topk + t * a.k;
+  if constexpr (kCluster > 1) {
+    // The take keys sit unordered in CTA 0's s_keys.  Each CTA copies them, then ranks its share
+    // [lo, hi): a key's output position is the number of keys above it (keys of one entry, which
+    // are equal, in their order in the buffer).  G threads (a power of two, aligned lanes of a
+    // warp) count one key's rank over every G-th key, and their sum places it.
+    cluster_sync_all();   // 4: CTA 0's s_keys[0, take) are the selected keys
+    const uint32_t src = mapa_cluster(smem_u32(s_keys), 0u);
+    {
+      constexpr int kPer = kIdxTopkMax / kThreads;
+      unsigned long long v[kPer];   // all loads in flight before the stores
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int i = tid + m * kThreads;
+        v[m] = i < (int)take ? ld_cluster_u64(src + 8u * (uint32_t)i) : 0ull;
+      }
+#pragma unroll
+      for (int m = 0; m < kPer; ++m)
+        if (tid + m * kThreads < (int)take) s_cand[tid + m * kThreads] = v[m];
+    }
+    cluster_arrive();   // 5 (arrival): this CTA no longer reads CTA 0's memory
+    __syncthreads();
+    const int per = ((int)take + kCluster - 1) / kCluster;
+    const int lo = min((int)take, rank * per), hi = min((int)take, lo + per);
+    int G = 1;
+    while (G < 32 && 2 * G * per <= kThreads) G <<= 1;
+    const int mine = lo + tid / G;   // the key this thread helps rank
+    const int gl = tid & (G - 1);
+    unsigned int above = 0;
+    if (mine < hi) {
+      const unsigned long long key = s_cand[mine];
+      for (int j = gl; j < (int)take; j += G) {
+        const unsigned long long o = s_cand[j];
+        above += (o > key || (o == key && j < mine)) ? 1u : 0u;
+      }
+    }
+    for (int o = 1; o < G; o <<= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+    if (mine < hi && gl == 0)
+      out[above] = (int32_t)(0xFFFFFFFFu - (uint32_t)(s_cand[mine] & 0xFFFFFFFFull));
+    for (int i = (int)take + rank * kThreads + tid; i < a.k; i += kThreads * kCluster) out[i] = -1;
+    cluster_wait();   // 5: no CTA reads this CTA's memory any more
+    return;
+  }
+
   // bitonic sort (descending) of the take keys, padded with zeros to a power of two.  Stages of
   // stride 32 and more exchange through shared memory, one barrier each; for every size the stages
   // of stride below 32 pair elements of one warp (n is a multiple of the warp's 32 elements, or
@@ -354,7 +421,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     __syncthreads();
   }
 
-  int32_t* out = a.topk + t * a.k;
   for (int i = tid; i < a.k; i += kThreads)
     out[i] = i < (int)take ? (int32_t)(0xFFFFFFFFu - (uint32_t)(s_keys[i] & 0xFFFFFFFFull)) : -1;
 }
