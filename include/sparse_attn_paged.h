@@ -20,6 +20,11 @@
  * path", part 1): the K scale multiplies the scores, the V scale multiplies the probabilities
  * before the PV product, and the softmax denominator accumulates the unscaled probabilities.
  *
+ * Stream order: every call is asynchronous on its stream and ordered after the work enqueued
+ * before it.  Calls whose grids take at most half the SMs launch with programmatic dependent
+ * launch: their CTAs may be resident and set up while the kernel before them in the stream still
+ * runs, but they read and write no global memory until that kernel has completed.
+ *
  * Memory layout (all device pointers are owned by the caller; the library never allocates,
  * frees or keeps a pointer after a call returns, and never synchronises the stream except in
  * sparse_attn_paged_check_errors):

@@ -136,6 +136,43 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).  A grid launched with
+// programmatic stream serialization may start while the grid before it in the stream still runs:
+// pdl_launch_dependents() lets the next grid start (once every CTA of this one has run it or
+// exited), and pdl_wait() returns once the grid before has completed and its memory operations
+// are visible (at once when the launch had no such predecessor).  A kernel runs pdl_wait() in
+// every thread before its first global memory access, so it reads and writes nothing that the
+// grid before it may still touch.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The launch attribute that allows it.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a = {};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+// A launch with that attribute when `pdl`.  The launchers set it when a grid has at most half as
+// many CTAs as there are SMs, so that the next grid can set up on idle SMs while this one runs.
+// A larger grid would instead have its CTAs placed where the grid before it leaves room, beside
+// its CTAs or in the order they finish (measured slower: the indexer's 128-CTA decode grid, the
+// attention's prefill grid).
+template <typename Kern, typename... Args>
+inline cudaError_t launch_with_pdl(Kern kern, dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, bool pdl, const Args&... args) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = stream;
+  cudaLaunchAttribute at[1] = {pdl_attribute()};
+  c.attrs = at;
+  c.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&c, kern, args...);
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

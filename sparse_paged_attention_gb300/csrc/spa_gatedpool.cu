@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kGatedPoolMaxWarps * 32)
   const int c0 = (int)(blockIdx.x % chunks) * CH;
   const int d = c0 + lane * VEC;
   const bool live = d < g.D;  // the vector path needs D % VEC == 0, so d + VEC - 1 < D too
+  pdl_launch_dependents();
+  pdl_wait();   // nothing global before the grid before this one is done
 
   float m[VEC], l[VEC], acc[VEC];
 #pragma unroll
@@ -144,11 +146,12 @@ cudaError_t launch_gated_pool(const GatedPoolArgs& g, int num_sms, cudaStream_t 
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   int nw = (g.R + kRowsPerBatch - 1) / kRowsPerBatch;  // about one batch of rows per warp
   nw = nw < 1 ? 1 : (nw > kGatedPoolMaxWarps ? kGatedPoolMaxWarps : nw);
+  const bool pdl = 2 * blocks <= num_sms;
   if (vec == 4)
-    gated_pool_kernel<4><<<(unsigned)blocks, nw * 32, 0, stream>>>(g);
-  else
-    gated_pool_kernel<1><<<(unsigned)blocks, nw * 32, 0, stream>>>(g);
-  return cudaGetLastError();
+    return launch_with_pdl(gated_pool_kernel<4>, dim3((unsigned)blocks), dim3(nw * 32), 0, stream,
+                           pdl, g);
+  return launch_with_pdl(gated_pool_kernel<1>, dim3((unsigned)blocks), dim3(nw * 32), 0, stream,
+                         pdl, g);
 }
 
 }  // namespace spa

@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm) indexer_kernel(con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
+  pdl_wait();   // nothing global before the grid before this one is done
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + L.bar_off + 8);
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -260,11 +262,12 @@ cudaError_t launch_indexer(const IndexerArgs& a, bool cand, int num_sms, cudaStr
   if (per_sm < 1) per_sm = 1;
   const long long cap = (long long)per_sm * num_sms;
   const long long grid = a.nunits < cap ? a.nunits : cap;
+  const bool pdl = 2 * grid <= num_sms;
   if (cand)
-    indexer_kernel<true><<<(unsigned)grid, kIdxThreads, smem, stream>>>(a);
-  else
-    indexer_kernel<false><<<(unsigned)grid, kIdxThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+    return launch_with_pdl(indexer_kernel<true>, dim3((unsigned)grid), dim3(kIdxThreads),
+                           (size_t)smem, stream, pdl, a);
+  return launch_with_pdl(indexer_kernel<false>, dim3((unsigned)grid), dim3(kIdxThreads),
+                         (size_t)smem, stream, pdl, a);
 }
 
 }  // namespace spa

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kKvwThreads, kKvwCtasPerSm) kv_write_kernel(co
 #define EMPTY(s) (ring + (uint32_t)ring_bytes + 8u * (uint32_t)(kKvwStages + (s)))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long n_groups = ((long long)a.T + kKvwGroup - 1) / kKvwGroup;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKvwStages; ++s) {
       mbar_init(FULL(s), 1);                 // the producer's armed arrival
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(kKvwThreads, kKvwCtasPerSm) kv_write_kernel(co
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();   // nothing global before the grid before this one is done
 
   if (warp == kKvwGroup) {
     // ---- producer: group g's K rows and V rows into stage (local group index) % kKvwStages ----
@@ -230,8 +232,8 @@ cudaError_t launch_kv_write(const KvWriteArgs& a, bool fp8, cudaStream_t stream)
   const long long groups = ((long long)a.T + kKvwGroup - 1) / kKvwGroup;
   const long long cap = (long long)sms * kKvwCtasPerSm;
   const unsigned blocks = (unsigned)(groups < cap ? groups : cap);
-  kern<<<blocks, kKvwThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_with_pdl(kern, dim3(blocks), dim3(kKvwThreads), (size_t)smem, stream,
+                         2LL * blocks <= sms, a);
 }
 
 }  // namespace spa

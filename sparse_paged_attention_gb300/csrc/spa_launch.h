@@ -28,6 +28,7 @@ struct AttnParams {
   int decode;           // 1: write split partials to ws_o / ws_lse for the merge kernel
   int cluster;          // > 1: the n_splits CTAs of one (token, head group) form a thread-block
                         // cluster and merge their partials through distributed shared memory
+  int pdl;              // 1: launched with programmatic dependent launch (set by the launcher)
 };
 
 // Kernel launch configuration: 4 softmax warps, 1 MMA warp, the gather warps and 1 resolver

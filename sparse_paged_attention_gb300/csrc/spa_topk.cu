@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
     }
   };
 
+  pdl_launch_dependents();
   // ---- pass 1: scored count, histogram of the top 12 bits ----
   for (int i = tid; i < kBins; i += kThreads) s_hist[i] = 0u;
   if (tid == 0) {
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
     s_eq_taken = 0;
   }
   __syncthreads();
+  pdl_wait();   // nothing global before the grid before this one is done
   unsigned int mine = 0;
   for (int c0 = cbeg; c0 < cend; c0 += kThreads * kUnroll) {
     uint32_t o[kUnroll];
@@ -428,24 +430,25 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
 // One row per cluster of kCluster CTAs.
 template <int kThreads, int kUnroll, int kCluster>
 cudaError_t launch_topk_cluster(const TopkArgs& a, cudaStream_t stream, bool query_only,
-                                int* max_clusters) {
+                                int* max_clusters, int sms) {
   const auto kern = topk_kernel<kThreads, kUnroll, kCluster>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && kCluster > 8)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t c = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = kCluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1] = pdl_attribute();
   c.gridDim = dim3((unsigned)(a.T * kCluster));
   c.blockDim = dim3(kThreads);
   c.dynamicSmemBytes = kSmemBytes;
   c.stream = stream;
   c.attrs = at;
-  c.numAttrs = 1;
+  c.numAttrs = (query_only || 2LL * a.T * kCluster > sms) ? 1 : 2;
   if (query_only) return cudaOccupancyMaxActiveClusters(max_clusters, kern, &c);
   return cudaLaunchKernelEx(&c, kern, a);
 }
@@ -465,19 +468,22 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if ((long long)a.T * 16 <= sms && dev < 64) {
     if (c16_fits[dev] == 0) {
       int n = 0;
-      e = launch_topk_cluster<512, 8, 16>(a, stream, true, &n);
+      e = launch_topk_cluster<512, 8, 16>(a, stream, true, &n, sms);
       if (e != cudaSuccess) (void)cudaGetLastError();
       c16_fits[dev] = (e == cudaSuccess && n >= 1) ? 1 : 2;
     }
-    if (c16_fits[dev] == 1) return launch_topk_cluster<512, 8, 16>(a, stream, false, nullptr);
+    if (c16_fits[dev] == 1)
+      return launch_topk_cluster<512, 8, 16>(a, stream, false, nullptr, sms);
   }
-  if ((long long)a.T * 8 <= sms) return launch_topk_cluster<512, 16, 8>(a, stream, false, nullptr);
+  if ((long long)a.T * 8 <= sms)
+    return launch_topk_cluster<512, 16, 8>(a, stream, false, nullptr, sms);
   const bool few = a.T < sms;
   const auto kern = few ? topk_kernel<1024, 16, 1> : topk_kernel<512, 8, 1>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)a.T, few ? 1024 : 512, kSmemBytes, stream>>>(a);
-  return cudaGetLastError();
+  const bool pdl = 2LL * a.T <= sms;
+  return launch_with_pdl(kern, dim3((unsigned)a.T), dim3(few ? 1024 : 512), (size_t)kSmemBytes,
+                         stream, pdl, a);
 }
 
 }  // namespace spa
