@@ -386,14 +386,29 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
   }
 
   // bitonic sort (descending) of the take keys, padded with zeros to a power of two.  Stages of
-  // stride 32 and more exchange through shared memory, one barrier each; for every size the stages
-  // of stride below 32 pair elements of one warp (n is a multiple of the warp's 32 elements, or
-  // one warp holds it all) and run together in registers, with shuffles, behind one barrier.
+  // stride 32 and more exchange through shared memory, one barrier each; the stages of stride
+  // below 32 pair elements of one warp and run together in registers, with shuffles, behind one
+  // barrier: all of sizes 2 .. 32 in one pass, then those of each larger size.
   int n = 1;
   while (n < (int)take) n <<= 1;
-  for (int i = (int)take + tid; i < n; i += kThreads) s_keys[i] = 0ull;
+  // sizes 2 .. min(n, 32): every stage of these pairs elements of one warp, so they all run in
+  // registers in one pass (the padding past take enters as zero keys)
+  const int n_reg = n < 32 ? n : 32;
+  for (int i0 = warp * 32; i0 < n; i0 += kThreads) {   // warp-uniform bounds
+    const int i = i0 + lane;
+    unsigned long long x = i < (int)take ? s_keys[i] : 0ull;
+    for (int size = 2; size <= n_reg; size <<= 1) {
+      const bool desc = (i & size) == 0;
+      for (int st = size >> 1; st > 0; st >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, st);
+        const bool lower = (lane & st) == 0;         // element i is the pair's first
+        x = (lower == desc) ? (x > y ? x : y) : (x < y ? x : y);
+      }
+    }
+    if (i < n) s_keys[i] = x;
+  }
   __syncthreads();
-  for (int size = 2; size <= n; size <<= 1) {
+  for (int size = 64; size <= n; size <<= 1) {
     int stride = size >> 1;
     for (; stride >= 32; stride >>= 1) {
       for (int i = tid; i < n; i += kThreads) {
