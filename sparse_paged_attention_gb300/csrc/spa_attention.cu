@@ -1574,15 +1574,16 @@ cudaError_t launch_attn(const AttnParams& p_in, int grid, bool fp8, cudaStream_t
   // enough that walking the page tables is a real share of an item (a single window tile is not)
   const bool res = grid < p.n_items && p.rs.W + p.rs.K >= 256;
   const bool tma = attn_uses_tma(grid, p.n_items, fp8, p.D);
-  // Programmatic dependent launch when two such grids fit on the GPU side by side (one CTA an
-  // SM): the next grid then sets up on idle SMs while this one runs (decode B1: 13.9 -> 13.3 us
-  // a call in a CUDA graph).  A grid that fills the GPU would instead be placed SM by SM in the
-  // order the one before it finishes (prefill S2048 in a graph: 299 -> 320 us), so it is not.
+  // Programmatic dependent launch for grids of at most a quarter of the SMs (one CTA an SM): the
+  // next grid then sets up on idle SMs while this one runs (decode B1, 32 CTAs: 13.9 -> 13.3 us a
+  // call in a CUDA graph).  At 64 CTAs (decode B8) it measured 0.1-0.25 us slower; a grid that
+  // fills the GPU would be placed SM by SM in the order the one before it finishes (prefill S2048
+  // in a graph: 299 -> 320 us).
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  p.pdl = 2 * grid <= sms ? 1 : 0;
+  p.pdl = 4 * grid <= sms ? 1 : 0;
   cudaLaunchConfig_t c = attn_config(grid, p.cluster, stream, attr, tma, res, p.pdl != 0);
   switch (attn_variant(fp8, res, tma)) {
     case 0: return cudaLaunchKernelEx(&c, attn_kernel<true, false, false>, p);
