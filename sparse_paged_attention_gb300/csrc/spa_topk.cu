@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
     if (tid == 0) {
       unsigned int v[kCluster];
 #pragma unroll
-      for (int k = 0; k < kCluster; ++k) v[k] = ld_cluster_u32(mapa_cluster(smem_u32(&s_count), (uint32_t)k));
+      for (int k = 0; k < kCluster; ++k)
+        v[k] = ld_cluster_u32(mapa_cluster(smem_u32(&s_count), (uint32_t)k));
       unsigned int tot = 0;
 #pragma unroll
       for (int k = 0; k < kCluster; ++k) tot += v[k];
@@ -243,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
   const auto bucket_keep = [&](unsigned long long key) {
     if constexpr (kCluster > 1) {
       const unsigned int slot = atom_add_cluster(mapa_cluster(smem_u32(&s_ncand), 0u), 1u);
-      if (slot < (unsigned int)kCandMax) st_cluster_u64(mapa_cluster(smem_u32(&s_cand[slot]), 0u), key);
+      if (slot < (unsigned int)kCandMax)
+        st_cluster_u64(mapa_cluster(smem_u32(&s_cand[slot]), 0u), key);
     } else {
       const unsigned int slot = atomicAdd(&s_ncand, 1u);
       if (slot < (unsigned int)kCandMax) s_cand[slot] = key;
@@ -278,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, kCluster > 1 ? 2 : (kThreads == 512 
         row_ords(c0, o, a.ncols);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-          if (o[u] != 0u && (o[u] >> kBinShift32) == bucket) f(topk_key(o[u], entry_of(col_of(c0, u))));
+          if (o[u] != 0u && (o[u] >> kBinShift32) == bucket)
+            f(topk_key(o[u], entry_of(col_of(c0, u))));
       }
     };
     // radix select below the top 12 bits: keys whose top (64 - shift) bits exceed `prefix` are
@@ -447,7 +450,8 @@ template <int kThreads, int kUnroll, int kCluster>
 cudaError_t launch_topk_cluster(const TopkArgs& a, cudaStream_t stream, bool query_only,
                                 int* max_clusters, int sms) {
   const auto kern = topk_kernel<kThreads, kUnroll, kCluster>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && kCluster > 8)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;

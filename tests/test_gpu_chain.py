@@ -41,7 +41,8 @@ class Step:
         self.win = spa.PagedPool(g(w.win.kv), g(w.win.block_table), None, None)
         self.cmp = spa.PagedPool(g(w.cmp.kv), g(w.cmp.block_table), None, None)
         self.k_new, self.v_new = g(new.k), g(new.v)
-        self.xq, self.xw, self.keys, self.kbt = g(x.q), g(x.weights), g(x.key_pool), g(x.block_table)
+        self.xq, self.xw = g(x.q), g(x.weights)
+        self.keys, self.kbt = g(x.key_pool), g(x.block_table)
         self.ncols = x.num_cols
         assert self.ncols == (P + 1) // RATIO
         self.logits = torch.empty((1, self.ncols), dtype=torch.float32, device=dev)
