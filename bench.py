@@ -68,6 +68,7 @@ INDEXERS = {
 TOPK_SHAPES = {"topk_t1_n65536_k512": (1, 65536, 512), "topk_t128_n8192_k512": (128, 8192, 512),
                "topk_t2048_n32768_k512": (2048, 32768, 512)}
 FLUSH_BYTES = 512 << 20   # > 129 MB of L2
+E2E_CHUNK = 1024          # tokens a chunk of the host-buffer prefill (e2e)
 # a device-side wait enqueued before each timed call, so that the GPU is still busy with it while
 # the host enqueues the start event, the call and the end event: the events then bracket device
 # time only (about 100 us at GB300 clocks)
@@ -348,13 +349,26 @@ def time_graph(fn, reps=20, rounds=10):
 
 
 def time_e2e(r, steps, warmup, flush, dist=None):
-    """The same call from host buffers: pinned host -> device copies of q, the top-k lists and
-    the positions, the library call, the device -> host copy of out, all inside the timed region
-    (the pools are the resident KV cache)."""
+    """The same call from host buffers, every copy inside the timed region (the pools are the
+    resident KV cache).  Prefill goes through the library's host-buffer entry point
+    (sparse_attn_paged_prefill_host): q, the top-k lists and the positions from pinned host
+    memory and out back to it, a chunk of E2E_CHUNK tokens at a time, the copies in, kernels and
+    copies out of consecutive chunks overlapping.  Decode, a few hundred KB, copies with torch
+    around the device call."""
     import torch
     q_h = r.w.q.pin_memory()
     pos_h = r.w.positions.pin_memory()
     tk_h = r.w.topk_idx.pin_memory() if r.tk is not None else None
+    sot_h = r.w.seq_of_token.pin_memory() if r.w.seq_of_token is not None else None
+    h2d = q_h.numel() * 2 + pos_h.numel() * 4 + (tk_h.numel() * 4 if tk_h is not None else 0) + \
+        (sot_h.numel() * 4 if sot_h is not None else 0)
+    d2h = q_h.numel() * 2
+    if not r.w.decode:
+        w = r.w
+        step = r.spa.bind_prefill_host(q_h, r.win, r.cmp, tk_h, pos_h, window=w.window,
+                                       ratio=w.ratio, scale=w.scale, seq_of_token=sot_h,
+                                       chunk_tokens=E2E_CHUNK, fp8=w.fp8)
+        return time_calls(step, steps, warmup, flush, dist), h2d, d2h
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype, pin_memory=True)
     q_d, pos_d = torch.empty_like(r.q), torch.empty_like(r.pos)
     tk_d = torch.empty_like(r.tk) if r.tk is not None else None
@@ -369,10 +383,7 @@ def time_e2e(r, steps, warmup, flush, dist=None):
         call()
         out_h.copy_(out_d, non_blocking=True)
 
-    times = time_calls(step, steps, warmup, flush, dist)
-    h2d = q_h.numel() * 2 + pos_h.numel() * 4 + (tk_h.numel() * 4 if tk_h is not None else 0)
-    d2h = out_h.numel() * 2
-    return times, h2d, d2h
+    return time_calls(step, steps, warmup, flush, dist), h2d, d2h
 
 
 def measure_workload(name, device, steps, warmup, flush, peaks, graph=True):

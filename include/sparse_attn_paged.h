@@ -116,6 +116,39 @@ int sparse_attn_paged_prefill_fp8(const void* q, const spa_pool_t* win, const sp
                                   const spa_problem_t* prob, void* out, void* stream);
 
 /*
+ * Prefill from host buffers: the same result as sparse_attn_paged_prefill[_fp8], bit for bit,
+ * for a caller whose queries and output live in host memory (the pages' prefill is one attention
+ * call per chunk of tokens, FreeToken PR 633 "Call paths").
+ *   q_host, out_host          host [T][H][D] bf16, 16-byte aligned;
+ *   prob->positions, ->topk_idx, ->seq_of_token   host arrays (the other fields as above);
+ *   win, cmp                  device pools and block tables (the resident KV cache);
+ *   chunk_tokens              tokens per chunk (>= 1);
+ *   staging                   device memory, 256-byte aligned, of at least
+ *                             sparse_attn_paged_prefill_host_staging_size(prob, chunk_tokens) bytes.
+ * The tokens go through the staging memory a chunk at a time: each chunk's q, top-k lists and
+ * positions are copied in, attended and its output copied out, with the copies in, the kernels
+ * and the copies out of consecutive chunks overlapping on streams of the library's own (made
+ * on the first call on a device, kept for the process).  Every query's output depends only on
+ * its own inputs, hence the bit-for-bit equality.  Host memory should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously and overlap.
+ * Stream order: the work starts after what was enqueued on `stream` before the call, and what
+ * is enqueued on `stream` after it waits for all of it (out_host is complete once `stream` has
+ * reached that point).  Calls from several host threads are serialised.  Errors: those of
+ * sparse_attn_paged_prefill, SPA_ERR_SHAPE (chunk_tokens < 1), SPA_ERR_NULL / SPA_ERR_ALIGN /
+ * SPA_ERR_WORKSPACE for the staging memory.
+ */
+size_t sparse_attn_paged_prefill_host_staging_size(const spa_problem_t* prob,
+                                                   int32_t chunk_tokens);
+int sparse_attn_paged_prefill_host(const void* q_host, const spa_pool_t* win,
+                                   const spa_pool_t* cmp, const spa_problem_t* prob,
+                                   void* out_host, int32_t chunk_tokens, void* staging,
+                                   size_t staging_bytes, void* stream);
+int sparse_attn_paged_prefill_host_fp8(const void* q_host, const spa_pool_t* win,
+                                       const spa_pool_t* cmp, const spa_problem_t* prob,
+                                       void* out_host, int32_t chunk_tokens, void* staging,
+                                       size_t staging_bytes, void* stream);
+
+/*
  * Decode: split-K over the column set (FreeToken PR 633, call paths: the split-K decode kernel),
  * then a log-sum-exp merge of the per-split partials into out.  When the queries leave SMs idle,
  * the column set of each query is split over up to 16 CTAs that form one thread-block cluster and

@@ -23,7 +23,9 @@ __all__ = [
     "sparse_attn_paged_decode_workspace_size", "sparse_attn_paged_decode_noalloc",
     "sparse_attn_paged_resolve_columns", "sparse_attn_paged_kv_write",
     "sparse_attn_paged_kv_write_fp8", "sparse_attn_gated_pool", "sparse_attn_indexer_logits",
-    "sparse_attn_indexer_topk", "BoundCall", "bind_prefill", "bind_decode",
+    "sparse_attn_indexer_topk", "sparse_attn_paged_prefill_host",
+    "sparse_attn_paged_prefill_host_fp8", "BoundCall", "bind_prefill", "bind_prefill_host",
+    "bind_decode",
     "sparse_attn_paged_check_errors", "sparse_attn_paged_strerror", "SPA_STATUS",
 ]
 
@@ -85,6 +87,12 @@ def load_library():
     for name in ("sparse_attn_paged_decode", "sparse_attn_paged_decode_fp8"):
         f = getattr(lib, name)
         f.argtypes = [P, PP, PP, PR, P, P, ctypes.c_size_t, P]
+        f.restype = ctypes.c_int
+    lib.sparse_attn_paged_prefill_host_staging_size.argtypes = [PR, ctypes.c_int32]
+    lib.sparse_attn_paged_prefill_host_staging_size.restype = ctypes.c_size_t
+    for name in ("sparse_attn_paged_prefill_host", "sparse_attn_paged_prefill_host_fp8"):
+        f = getattr(lib, name)
+        f.argtypes = [P, PP, PP, PR, P, ctypes.c_int32, P, ctypes.c_size_t, P]
         f.restype = ctypes.c_int
     lib.sparse_attn_paged_decode_noalloc.argtypes = [P, PP, PP, PR, P, P]
     lib.sparse_attn_paged_decode_noalloc.restype = ctypes.c_int
@@ -305,6 +313,55 @@ def bind_prefill(q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_
                      stream)
     call.out = out
     return call
+
+
+def bind_prefill_host(q, win, cmp, topk_idx, positions, *, window, ratio, scale,
+                      seq_of_token=None, out=None, num_seqs=None, chunk_tokens=1024, staging=None,
+                      stream=None, fp8=False) -> BoundCall:
+    """``sparse_attn_paged_prefill_host[_fp8]`` on fixed tensors, as a zero-argument callable.
+
+    q, topk_idx, positions, seq_of_token and out are CPU tensors (page-locked, ``pin_memory()``,
+    for the copies to overlap); the pools are on the GPU.  The device staging memory is allocated
+    here once when not given.  ``call.out`` is complete once the call's stream has reached the
+    point after the call."""
+    lib = load_library()
+    _check_q(q)
+    for name, t in (("q", q), ("positions", positions), ("topk_idx", topk_idx),
+                    ("seq_of_token", seq_of_token), ("out", out)):
+        if t is not None and t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 host tensor shaped like q")
+    prob = _problem_c(q, win, topk_idx, positions, seq_of_token, window, ratio, scale, num_seqs)
+    if staging is None:
+        nbytes = int(lib.sparse_attn_paged_prefill_host_staging_size(ctypes.byref(prob),
+                                                                     int(chunk_tokens)))
+        staging = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=win.kv.device)
+    w, c = _pool_c(win, fp8), _pool_c(cmp, fp8)
+    fn = lib.sparse_attn_paged_prefill_host_fp8 if fp8 else lib.sparse_attn_paged_prefill_host
+    args = (q.data_ptr(), ctypes.byref(w), ctypes.byref(c) if c is not None else None,
+            ctypes.byref(prob), out.data_ptr(), int(chunk_tokens), staging.data_ptr(),
+            staging.numel() * staging.element_size())
+    call = BoundCall(fn, args, (q, win, cmp, topk_idx, positions, seq_of_token, out, staging,
+                                w, c, prob), stream)
+    call.out = out
+    call.staging = staging
+    return call
+
+
+def sparse_attn_paged_prefill_host(q, win, cmp, topk_idx, positions, **kw):
+    """Prefill from host tensors (q, top-k lists, positions, out on the CPU; pools on the GPU),
+    chunk by chunk through device staging memory, copies and kernels overlapping; returns the
+    host output (complete once the stream has passed the call: synchronise before reading)."""
+    call = bind_prefill_host(q, win, cmp, topk_idx, positions, **kw)
+    call()
+    return call.out
+
+
+def sparse_attn_paged_prefill_host_fp8(q, win, cmp, topk_idx, positions, **kw):
+    return sparse_attn_paged_prefill_host(q, win, cmp, topk_idx, positions, fp8=True, **kw)
 
 
 def bind_decode(q, win, cmp, topk_idx, positions, *, window, ratio, scale, seq_of_token=None,

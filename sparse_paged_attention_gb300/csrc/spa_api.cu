@@ -377,7 +377,155 @@ int kv_write(const void* k, const void* v, int32_t T, int32_t D, const int32_t* 
 }
 }  // namespace
 
+namespace {
+// ---- prefill from host buffers: chunks through a double-buffered device staging area ----
+// Per device: a stream each for the copies in, the kernels and the copies out, and the events
+// that order them; made on the first call, kept for the process.
+struct HostPipe {
+  bool ready;
+  cudaStream_t in, comp, out;
+  cudaEvent_t entry, exit, in_done[2], comp_done[2], out_done[2];
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of one staging slot (a chunk of tc tokens): q, out, top-k lists, positions,
+// sequence ids, each 256-byte aligned.
+struct HostSlot {
+  size_t q, out, topk, pos, seq, bytes;
+};
+HostSlot host_slot(const spa_problem_t* pr, long long tc) {
+  const size_t rows = (size_t)tc * (size_t)pr->num_heads * (size_t)pr->head_dim * 2;
+  HostSlot s;
+  s.q = 0;
+  s.out = round256(rows);
+  s.topk = s.out + round256(rows);
+  s.pos = s.topk + round256((size_t)tc * (size_t)pr->topk * 4);
+  s.seq = s.pos + round256((size_t)tc * 4);
+  s.bytes = s.seq + round256((size_t)tc * 4);
+  return s;
+}
+
+int host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t* st : {&hp.in, &hp.comp, &hp.out})
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&hp.entry, &hp.exit, &hp.in_done[0], &hp.in_done[1], &hp.comp_done[0],
+                            &hp.comp_done[1], &hp.out_done[0], &hp.out_done[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "host prefill streams");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return SPA_OK;
+}
+
+int prefill_host(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
+                 const spa_problem_t* pr, void* out, int32_t chunk, void* staging,
+                 size_t staging_bytes, void* stream, bool fp8) {
+  int st = validate(q, win, cmp, pr, out, fp8);
+  if (st) return st;
+  if (chunk < 1) return SPA_ERR_SHAPE;
+  if (pr->num_tokens == 0) return SPA_OK;
+  if (!staging) return SPA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(staging) % 256 != 0) return SPA_ERR_ALIGN;
+  const long long T = pr->num_tokens;
+  const long long tc = chunk < T ? chunk : T;
+  const HostSlot sl = host_slot(pr, tc);
+  if (staging_bytes < 2 * sl.bytes) return SPA_ERR_WORKSPACE;
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st) return st;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  st = host_pipe(dev, &hp);
+  if (st) return st;
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  const size_t qrow = (size_t)pr->num_heads * (size_t)pr->head_dim * 2;   // bytes of one token
+  const int K = pr->topk;
+  const auto H2D = cudaMemcpyHostToDevice;
+  cudaError_t e = cudaEventRecord(hp->entry, user);
+  for (cudaStream_t s : {hp->in, hp->comp, hp->out})
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->entry, 0);
+  int c = 0;
+  for (long long c0 = 0; c0 < T && e == cudaSuccess && st == SPA_OK; c0 += tc, ++c) {
+    const long long n = tc < T - c0 ? tc : T - c0;
+    const int slot = c & 1;
+    uint8_t* base = static_cast<uint8_t*>(staging) + (size_t)slot * sl.bytes;
+    // copies in, once the kernel of chunk c - 2 has read this slot
+    if (c >= 2) e = cudaStreamWaitEvent(hp->in, hp->comp_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(base + sl.q, static_cast<const uint8_t*>(q) + (size_t)c0 * qrow,
+                          (size_t)n * qrow, H2D, hp->in);
+    if (e == cudaSuccess && K > 0)
+      e = cudaMemcpyAsync(base + sl.topk, pr->topk_idx + (size_t)c0 * K, (size_t)n * K * 4, H2D,
+                          hp->in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(base + sl.pos, pr->positions + c0, (size_t)n * 4, H2D, hp->in);
+    if (e == cudaSuccess && pr->seq_of_token)
+      e = cudaMemcpyAsync(base + sl.seq, pr->seq_of_token + c0, (size_t)n * 4, H2D, hp->in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in_done[slot], hp->in);
+    // the chunk's attention, once its inputs are in and the copy out of chunk c - 2 is done
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0);
+    if (e == cudaSuccess && c >= 2) e = cudaStreamWaitEvent(hp->comp, hp->out_done[slot], 0);
+    if (e != cudaSuccess) break;
+    spa_problem_t cp = *pr;
+    cp.num_tokens = (int32_t)n;
+    cp.positions = reinterpret_cast<const int32_t*>(base + sl.pos);
+    cp.topk_idx = K > 0 ? reinterpret_cast<const int32_t*>(base + sl.topk) : nullptr;
+    cp.seq_of_token = pr->seq_of_token ? reinterpret_cast<const int32_t*>(base + sl.seq) : nullptr;
+    st = run(base + sl.q, win, cmp, &cp, base + sl.out, nullptr, 0, hp->comp, false, fp8);
+    if (st != SPA_OK) break;
+    e = cudaEventRecord(hp->comp_done[slot], hp->comp);
+    // copy out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->comp_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + (size_t)c0 * qrow, base + sl.out,
+                          (size_t)n * qrow, cudaMemcpyDeviceToHost, hp->out);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->out_done[slot], hp->out);
+  }
+  // the caller's stream resumes after everything enqueued here, also after a failure part way
+  for (cudaStream_t s : {hp->in, hp->comp, hp->out}) {
+    cudaError_t e2 = cudaEventRecord(hp->exit, s);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(user, hp->exit, 0);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (st != SPA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "host prefill copies");
+  return SPA_OK;
+}
+}  // namespace
+
 extern "C" {
+
+size_t sparse_attn_paged_prefill_host_staging_size(const spa_problem_t* prob,
+                                                   int32_t chunk_tokens) {
+  if (!prob || prob->num_tokens < 0 || prob->num_heads < 1 || prob->head_dim < 1 ||
+      prob->topk < 0 || chunk_tokens < 1)
+    return 0;
+  const long long tc = chunk_tokens < prob->num_tokens ? chunk_tokens : prob->num_tokens;
+  return 2 * host_slot(prob, tc > 0 ? tc : 1).bytes;
+}
+
+int sparse_attn_paged_prefill_host(const void* q_host, const spa_pool_t* win,
+                                   const spa_pool_t* cmp, const spa_problem_t* prob,
+                                   void* out_host, int32_t chunk_tokens, void* staging,
+                                   size_t staging_bytes, void* stream) {
+  return prefill_host(q_host, win, cmp, prob, out_host, chunk_tokens, staging, staging_bytes,
+                      stream, false);
+}
+
+int sparse_attn_paged_prefill_host_fp8(const void* q_host, const spa_pool_t* win,
+                                       const spa_pool_t* cmp, const spa_problem_t* prob,
+                                       void* out_host, int32_t chunk_tokens, void* staging,
+                                       size_t staging_bytes, void* stream) {
+  return prefill_host(q_host, win, cmp, prob, out_host, chunk_tokens, staging, staging_bytes,
+                      stream, true);
+}
 
 int sparse_attn_paged_prefill(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
                               const spa_problem_t* prob, void* out, void* stream) {

@@ -191,3 +191,35 @@ def test_header_is_plain_c_and_every_entry_point_links(lib, tmp_path):
     assert out.returncode == 0, out.stderr
     n, version = out.stdout.split(" ", 1)
     assert int(n) == len(names) and "sm_103a" in version
+
+
+def test_host_prefill_staging_and_argument_checks(lib, no_device):
+    """The host-buffer prefill: the staging size of a chunk (two slots, each q and out chunks in
+    bf16, the top-k lists, positions and sequence ids, every part 256-byte aligned), and the
+    argument checks made before any device work."""
+    S = spa.SPA_STATUS
+    T, H, D, K, chunk = 8192, 64, 512, 512, 1024
+    prob = SpaProblemC(T, 1, H, D, 128, K, 4, 0.04, 0x6000, None, 0x7000)
+    rows = chunk * H * D * 2                           # 64 MiB of bf16 rows per chunk
+    slot = 2 * rows + chunk * K * 4 + 2 * 4096          # q, out, top-k lists, positions, seq ids
+    assert lib.sparse_attn_paged_prefill_host_staging_size(ctypes.byref(prob), chunk) == 2 * slot
+    # a chunk larger than the call is cut to the call; 3 tokens of 4-byte arrays take 256 bytes
+    small = SpaProblemC(3, 1, 8, 64, 16, 32, 4, 0.1, 0x6000, None, 0x7000)
+    assert lib.sparse_attn_paged_prefill_host_staging_size(ctypes.byref(small), 1000) == \
+        2 * (2 * 3072 + 512 + 256 + 256)
+    assert lib.sparse_attn_paged_prefill_host_staging_size(ctypes.byref(prob), 0) == 0
+    assert lib.sparse_attn_paged_prefill_host_staging_size(None, chunk) == 0
+    pool, cpool, pr, q, out = _args()
+    f = lib.sparse_attn_paged_prefill_host
+    need = lib.sparse_attn_paged_prefill_host_staging_size(ctypes.byref(pr), 64)
+    call = lambda chunk, st, nbytes: f(q, ctypes.byref(pool), ctypes.byref(cpool),
+                                       ctypes.byref(pr), out, chunk, st, nbytes, None)
+    assert call(0, 0x100000, need) == S["SPA_ERR_SHAPE"]
+    assert call(64, None, need) == S["SPA_ERR_NULL"]
+    assert call(64, 0x100010, need) == S["SPA_ERR_ALIGN"]          # 16- but not 256-byte aligned
+    assert call(64, 0x100000, need - 1) == S["SPA_ERR_WORKSPACE"]
+    assert f(q, ctypes.byref(pool), ctypes.byref(cpool), None, out, 64, 0x100000, need,
+             None) == S["SPA_ERR_NULL"]
+    assert lib.sparse_attn_paged_prefill_host_fp8(q, ctypes.byref(pool), ctypes.byref(cpool),
+                                                  ctypes.byref(pr), out, 64, 0x100000, need,
+                                                  None) == S["SPA_ERR_NULL"]   # fp8 needs scales
