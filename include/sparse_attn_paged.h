@@ -124,11 +124,14 @@ int sparse_attn_paged_prefill_fp8(const void* q, const spa_pool_t* win, const sp
  *   win, cmp                  device pools and block tables (the resident KV cache);
  *   chunk_tokens              tokens per chunk (>= 1);
  *   staging                   device memory, 256-byte aligned, of at least
- *                             sparse_attn_paged_prefill_host_staging_size(prob, chunk_tokens) bytes.
- * The tokens go through the staging memory a chunk at a time: each chunk's q, top-k lists and
- * positions are copied in, attended and its output copied out, with the copies in, the kernels
- * and the copies out of consecutive chunks overlapping on streams of the library's own (made
- * on the first call on a device, kept for the process).  Every query's output depends only on
+ *                             sparse_attn_paged_prefill_host_staging_size(prob, chunk_tokens) bytes
+ *                             (two slots of one chunk's q, out, top-k lists, positions and
+ *                             sequence ids).
+ * The tokens go through the staging memory a chunk at a time (a quarter of chunk_tokens first and
+ * last, chunk_tokens between): each chunk's q, top-k lists and positions are copied in, attended
+ * and its output copied out, with the copies in, the kernels and the copies out of consecutive
+ * chunks overlapping on streams of the library's own (made on the first call on a device, kept
+ * for the process).  Every query's output depends only on
  * its own inputs, hence the bit-for-bit equality.  Host memory should be page-locked
  * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously and overlap.
  * Stream order: the work starts after what was enqueued on `stream` before the call, and what

@@ -378,13 +378,14 @@ int kv_write(const void* k, const void* v, int32_t T, int32_t D, const int32_t* 
 }  // namespace
 
 namespace {
-// ---- prefill from host buffers: chunks through a double-buffered device staging area ----
+// ---- prefill from host buffers: chunks through a device staging area of kHostSlots slots ----
+constexpr int kHostSlots = 2;   // (three measured the same)
 // Per device: a stream each for the copies in, the kernels and the copies out, and the events
 // that order them; made on the first call, kept for the process.
 struct HostPipe {
   bool ready;
   cudaStream_t in, comp, out;
-  cudaEvent_t entry, exit, in_done[2], comp_done[2], out_done[2];
+  cudaEvent_t entry, exit, in_done[kHostSlots], comp_done[kHostSlots], out_done[kHostSlots];
 };
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;
@@ -414,9 +415,11 @@ int host_pipe(int dev, HostPipe** out) {
     cudaError_t e = cudaSuccess;
     for (cudaStream_t* st : {&hp.in, &hp.comp, &hp.out})
       if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
-    for (cudaEvent_t* ev : {&hp.entry, &hp.exit, &hp.in_done[0], &hp.in_done[1], &hp.comp_done[0],
-                            &hp.comp_done[1], &hp.out_done[0], &hp.out_done[1]})
+    for (cudaEvent_t* ev : {&hp.entry, &hp.exit})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (int i = 0; i < kHostSlots; ++i)
+      for (cudaEvent_t* ev : {&hp.in_done[i], &hp.comp_done[i], &hp.out_done[i]})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(e, "host prefill streams");
     hp.ready = true;
   }
@@ -436,7 +439,7 @@ int prefill_host(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
   const long long T = pr->num_tokens;
   const long long tc = chunk < T ? chunk : T;
   const HostSlot sl = host_slot(pr, tc);
-  if (staging_bytes < 2 * sl.bytes) return SPA_ERR_WORKSPACE;
+  if (staging_bytes < kHostSlots * sl.bytes) return SPA_ERR_WORKSPACE;
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
   if (st) return st;
@@ -451,13 +454,23 @@ int prefill_host(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
   cudaError_t e = cudaEventRecord(hp->entry, user);
   for (cudaStream_t s : {hp->in, hp->comp, hp->out})
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->entry, 0);
+  // Chunk sizes: a quarter chunk first and last, so that the pipeline fills and drains sooner
+  // (nothing overlaps the first chunk's copy in, nor the last chunk's kernel and copy out), full
+  // chunks between.
+  const long long quarter = tc / 4 > 0 ? tc / 4 : 1;
+  const auto chunk_at = [&](long long c0) -> long long {
+    const long long rest = T - c0;
+    if (c0 == 0) return quarter < rest ? quarter : rest;
+    if (rest > tc + quarter) return tc;
+    return rest >= 2 * quarter ? rest - quarter : rest;   // (both at most tc)
+  };
   int c = 0;
-  for (long long c0 = 0; c0 < T && e == cudaSuccess && st == SPA_OK; c0 += tc, ++c) {
-    const long long n = tc < T - c0 ? tc : T - c0;
-    const int slot = c & 1;
+  for (long long c0 = 0, n = 0; c0 < T && e == cudaSuccess && st == SPA_OK; c0 += n, ++c) {
+    n = chunk_at(c0);
+    const int slot = c % kHostSlots;
     uint8_t* base = static_cast<uint8_t*>(staging) + (size_t)slot * sl.bytes;
-    // copies in, once the kernel of chunk c - 2 has read this slot
-    if (c >= 2) e = cudaStreamWaitEvent(hp->in, hp->comp_done[slot], 0);
+    // copies in, once the kernel of the chunk kHostSlots back has read this slot
+    if (c >= kHostSlots) e = cudaStreamWaitEvent(hp->in, hp->comp_done[slot], 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(base + sl.q, static_cast<const uint8_t*>(q) + (size_t)c0 * qrow,
                           (size_t)n * qrow, H2D, hp->in);
@@ -469,9 +482,10 @@ int prefill_host(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
     if (e == cudaSuccess && pr->seq_of_token)
       e = cudaMemcpyAsync(base + sl.seq, pr->seq_of_token + c0, (size_t)n * 4, H2D, hp->in);
     if (e == cudaSuccess) e = cudaEventRecord(hp->in_done[slot], hp->in);
-    // the chunk's attention, once its inputs are in and the copy out of chunk c - 2 is done
+    // the chunk's attention, once its inputs are in and the slot's previous copy out is done
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in_done[slot], 0);
-    if (e == cudaSuccess && c >= 2) e = cudaStreamWaitEvent(hp->comp, hp->out_done[slot], 0);
+    if (e == cudaSuccess && c >= kHostSlots)
+      e = cudaStreamWaitEvent(hp->comp, hp->out_done[slot], 0);
     if (e != cudaSuccess) break;
     spa_problem_t cp = *pr;
     cp.num_tokens = (int32_t)n;
@@ -508,7 +522,7 @@ size_t sparse_attn_paged_prefill_host_staging_size(const spa_problem_t* prob,
       prob->topk < 0 || chunk_tokens < 1)
     return 0;
   const long long tc = chunk_tokens < prob->num_tokens ? chunk_tokens : prob->num_tokens;
-  return 2 * host_slot(prob, tc > 0 ? tc : 1).bytes;
+  return kHostSlots * host_slot(prob, tc > 0 ? tc : 1).bytes;
 }
 
 int sparse_attn_paged_prefill_host(const void* q_host, const spa_pool_t* win,

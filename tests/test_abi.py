@@ -194,8 +194,8 @@ def test_header_is_plain_c_and_every_entry_point_links(lib, tmp_path):
 
 
 def test_host_prefill_staging_and_argument_checks(lib, no_device):
-    """The host-buffer prefill: the staging size of a chunk (two slots, each q and out chunks in
-    bf16, the top-k lists, positions and sequence ids, every part 256-byte aligned), and the
+    """The host-buffer prefill: the staging size of a chunk (two slots, each q and out chunks
+    in bf16, the top-k lists, positions and sequence ids, every part 256-byte aligned), and the
     argument checks made before any device work."""
     S = spa.SPA_STATUS
     T, H, D, K, chunk = 8192, 64, 512, 512, 1024
