@@ -454,19 +454,12 @@ int prefill_host(const void* q, const spa_pool_t* win, const spa_pool_t* cmp,
   cudaError_t e = cudaEventRecord(hp->entry, user);
   for (cudaStream_t s : {hp->in, hp->comp, hp->out})
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->entry, 0);
-  // Chunk sizes: a quarter chunk first and last, so that the pipeline fills and drains sooner
-  // (nothing overlaps the first chunk's copy in, nor the last chunk's kernel and copy out), full
-  // chunks between.
-  const long long quarter = tc / 4 > 0 ? tc / 4 : 1;
-  const auto chunk_at = [&](long long c0) -> long long {
-    const long long rest = T - c0;
-    if (c0 == 0) return quarter < rest ? quarter : rest;
-    if (rest > tc + quarter) return tc;
-    return rest >= 2 * quarter ? rest - quarter : rest;   // (both at most tc)
-  };
+  // chunk sizes (spa_plan.h): a quarter chunk first and last, so that the pipeline fills and
+  // drains sooner (nothing overlaps the first chunk's copy in, nor the last chunk's kernel and
+  // copy out), full chunks between
   int c = 0;
   for (long long c0 = 0, n = 0; c0 < T && e == cudaSuccess && st == SPA_OK; c0 += n, ++c) {
-    n = chunk_at(c0);
+    n = spa::host_chunk_tokens(T, tc, c0);
     const int slot = c % kHostSlots;
     uint8_t* base = static_cast<uint8_t*>(staging) + (size_t)slot * sl.bytes;
     // copies in, once the kernel of the chunk kHostSlots back has read this slot

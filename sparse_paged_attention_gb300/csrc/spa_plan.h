@@ -1,7 +1,7 @@
 // spa_plan.h - host-side split arithmetic of the decode path that keeps its split-K partials in
-// global memory (a caller workspace, or the library's built-in scratch array), and the bytes those
-// partials take.  Plain C++ with no CUDA dependency, so that it can be compiled and checked on a
-// machine without a GPU.
+// global memory (a caller workspace, or the library's built-in scratch array), the bytes those
+// partials take, and the chunk schedule of the prefill from host buffers.  Plain C++ with no CUDA
+// dependency, so that it can be compiled and checked on a machine without a GPU.
 #pragma once
 
 #include <cstddef>
@@ -48,6 +48,18 @@ inline void plan_partials(int C, long long T, int H, int D, int sms, int max_spl
   }
   *cols = c;
   *splits = n;
+}
+
+// Chunk schedule of the prefill from host buffers: the tokens of the chunk that starts at token c0
+// of T, with chunks of at most tc tokens (1 <= tc <= T).  A quarter chunk first and last, so that
+// the copy pipeline fills and drains sooner, full chunks between; a tail shorter than two quarters
+// is one chunk.  Every size is in [1, tc] and the chunks cover [0, T) in order.
+inline long long host_chunk_tokens(long long T, long long tc, long long c0) {
+  const long long quarter = tc / 4 > 0 ? tc / 4 : 1;
+  const long long rest = T - c0;
+  if (c0 == 0) return quarter < rest ? quarter : rest;
+  if (rest > tc + quarter) return tc;
+  return rest >= 2 * quarter ? rest - quarter : rest;   // (both at most tc)
 }
 
 }  // namespace spa

@@ -68,3 +68,37 @@ def test_one_split_when_nothing_smaller_fits(plan_exe):
     # 64 tokens x 128 heads x 512: one split alone is 16 MiB of O plus the LSEs, over the cap
     (s, c, b), = _plan(plan_exe, [(640, 64, 128, 512, 152, MERGE_MAX_SPLITS, SCRATCH)])
     assert (s, c) == (1, 640) and b > SCRATCH
+
+
+@pytest.fixture(scope="module")
+def chunks_exe(tmp_path_factory):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    exe = tmp_path_factory.mktemp("chunks") / "host_chunks"
+    r = subprocess.run([cxx, "-std=c++17", "-O2", "-I",
+                        os.path.join(ROOT, "sparse_paged_attention_gb300", "csrc"),
+                        os.path.join(ROOT, "tests", "host_chunks.cpp"), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return str(exe)
+
+
+def test_host_prefill_chunks_cover_every_token_once(chunks_exe):
+    """The prefill from host buffers takes the tokens in order, a quarter chunk first and last
+    and full chunks between: the chunks cover [0, T) exactly, each holds 1 to tc tokens (what a
+    staging slot holds), and a long call is mostly full chunks."""
+    cases = [(T, min(chunk, T)) for T in (1, 2, 3, 5, 7, 100, 255, 256, 257, 577, 1025, 2048,
+                                          8191, 8192, 30001)
+             for chunk in (1, 2, 3, 4, 5, 7, 128, 192, 300, 512, 1024, 4096)]
+    text = "".join(f"{T} {tc}\n" for T, tc in cases)
+    out = subprocess.run([chunks_exe], input=text, capture_output=True, text=True, check=True)
+    lines = out.stdout.splitlines()
+    assert len(lines) == len(cases)
+    for (T, tc), line in zip(cases, lines):
+        sizes = [int(v) for v in line.split()]
+        assert sum(sizes) == T and all(1 <= n <= tc for n in sizes), (T, tc, sizes)
+        if T >= 4 * tc >= 16:
+            assert sizes[0] == tc // 4 and sizes.count(tc) >= len(sizes) - 3, (T, tc, sizes)
+    sizes = [int(v) for v in lines[cases.index((8192, 1024))].split()]
+    assert sizes == [256] + [1024] * 7 + [512, 256]
